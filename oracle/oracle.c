@@ -1,0 +1,405 @@
+/*
+ * oracle.c -- plain, slow, FP64 CPU oracle for paged block-sparse prefill attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load this
+ * file: only the tests, the package smoke check and the benchmark's CPU-baseline leg do.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * What it computes, step by step, straight from the definitions on the pages:
+ *
+ *   token metadata   request, absolute position t = ctx_len + i, own page o = t / page.
+ *   indexer          S[r][p] = max over the visible keys j of page p (j <= t) of q.k_j,
+ *                    the raw dot product (no softmax scale).  Only pages p <= o are written.
+ *                    ("MSA PR 36: Q8KV8 prefill indexer", Changes: per-page max; Wrapper API:
+ *                    score buffer [total_q * num_heads, >= max_pages] with a row pitch.)
+ *   top-k            the own page is always kept; the other min(k, o+1) - 1 pages are the
+ *                    best by (score descending, page ascending); emitted as an ascending
+ *                    set, padded with -1.  (north-star definition; "MSA PR 36", Validation:
+ *                    bitwise-stable top-k.)
+ *   inversion        for every (request, logical page, kv head) bucket, the ordered list of
+ *                    (row, slot) pairs that selected it, rows ascending.
+ *   forward          per (row, slot): softmax over the visible keys of the selected page,
+ *                    logits = scale * q.k; partial O = sum p v / l; LSE = m + ln l.  Only the
+ *                    own page is masked ("MSA PR 21", K1 Softmax bullet).
+ *   combine          per row: LSE-weighted merge of the k partials; an empty slot
+ *                    (lse = -inf) has weight exactly 0 ("MSA PR 21", Combine section).
+ *   dense            the direct definition: one softmax over the union of the selected
+ *                    pages' visible keys (used to cross-check forward + combine).
+ *   decode           BF16 / FP16 / E4M3 / NVFP4 (E2M1 code x E4M3 per-16 scale) bit-field
+ *                    decode from the format definitions ("MSA PR 21", Build the prefill for
+ *                    SM107: the code-times-scale product).
+ *
+ * Every sum is accumulated in double.  Functions take an optional row subset so that the
+ * full-size workloads can be checked on sampled rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_E4M3 = 2, ORC_NVFP4 = 3, ORC_FP32 = 4 };
+
+typedef struct {
+  int32_t batch;
+  const int32_t* q_lens;    /* [batch] */
+  const int32_t* ctx_lens;  /* [batch] */
+  int32_t num_q_heads;      /* H */
+  int32_t num_kv_heads;     /* H_kv */
+  int32_t head_dim;         /* D */
+  int32_t page_size;        /* P */
+  int32_t top_k;            /* k */
+  int32_t max_pages;        /* page-table row length */
+  int32_t num_phys_pages;
+  const int32_t* page_table; /* [batch][max_pages], logical -> physical */
+} orc_problem;
+
+typedef struct {
+  const void* data;    /* element bits */
+  const void* scales;  /* NVFP4 only: one E4M3 byte per 16 consecutive elements */
+  int32_t dtype;
+  double scale;        /* per-tensor multiplier applied after decoding */
+} orc_tensor;
+
+/* ---------------------------------------------------------------- decode */
+
+/* BF16: the upper 16 bits of an IEEE binary32. */
+double orc_decode_bf16(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double orc_decode_fp16(uint16_t b) {
+  int s = (b >> 15) & 1, e = (b >> 10) & 0x1f, m = b & 0x3ff;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp(1024.0 + m, e - 25);
+  return s ? -v : v;
+}
+
+/* OCP FP8 E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa; no infinities,
+ * S.1111.111 is NaN, the largest finite value is 448. */
+double orc_decode_e4m3(uint8_t b) {
+  int s = (b >> 7) & 1, e = (b >> 3) & 0xf, m = b & 0x7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(8.0 + m, e - 10);
+  return s ? -v : v;
+}
+
+/* OCP FP4 E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa; values 0, .5, 1, 1.5, 2, 3, 4, 6. */
+double orc_decode_e2m1(uint8_t nib) {
+  int s = (nib >> 3) & 1, e = (nib >> 1) & 0x3, m = nib & 1;
+  double v;
+  if (e == 0) v = 0.5 * m;
+  else v = ldexp(2.0 + m, e - 2);
+  return s ? -v : v;
+}
+
+/* Element i of a tensor, decoded and multiplied by the per-tensor scale. */
+static double elem(const orc_tensor* t, int64_t i) {
+  double v;
+  switch (t->dtype) {
+    case ORC_BF16: v = orc_decode_bf16(((const uint16_t*)t->data)[i]); break;
+    case ORC_FP16: v = orc_decode_fp16(((const uint16_t*)t->data)[i]); break;
+    case ORC_E4M3: v = orc_decode_e4m3(((const uint8_t*)t->data)[i]); break;
+    case ORC_NVFP4: {
+      /* two codes per byte, the even element in the low nibble */
+      uint8_t byte = ((const uint8_t*)t->data)[i >> 1];
+      uint8_t nib = (i & 1) ? (byte >> 4) : (byte & 0xf);
+      uint8_t sc = ((const uint8_t*)t->scales)[i >> 4];
+      v = orc_decode_e2m1(nib) * orc_decode_e4m3(sc);
+      break;
+    }
+    case ORC_FP32: v = (double)((const float*)t->data)[i]; break;
+    default: v = NAN;
+  }
+  return v * t->scale;
+}
+
+/* Decode n consecutive elements starting at element `first` into out[]. */
+void orc_decode(orc_tensor t, int64_t first, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = elem(&t, first + i);
+}
+
+/* ---------------------------------------------------------------- metadata */
+
+/* Per flat token: request index and absolute position t = ctx_len[req] + i. */
+int64_t orc_token_meta(const orc_problem* pb, int32_t* tok_req, int32_t* tok_pos) {
+  int64_t tok = 0;
+  for (int b = 0; b < pb->batch; ++b)
+    for (int i = 0; i < pb->q_lens[b]; ++i, ++tok) {
+      if (tok_req) tok_req[tok] = b;
+      if (tok_pos) tok_pos[tok] = pb->ctx_lens[b] + i;
+    }
+  return tok;
+}
+
+typedef struct { int32_t req, t, o, tok, h, g; } row_info;
+
+static row_info describe_row(const orc_problem* pb, int64_t r) {
+  row_info ri;
+  int64_t tok = r / pb->num_q_heads;
+  ri.h = (int)(r % pb->num_q_heads);
+  ri.g = ri.h / (pb->num_q_heads / pb->num_kv_heads);
+  ri.tok = (int)tok;
+  int64_t acc = 0;
+  ri.req = -1;
+  for (int b = 0; b < pb->batch; ++b) {
+    if (tok < acc + pb->q_lens[b]) { ri.req = b; ri.t = pb->ctx_lens[b] + (int)(tok - acc); break; }
+    acc += pb->q_lens[b];
+  }
+  ri.o = ri.t / pb->page_size;
+  return ri;
+}
+
+/* Flat element index of K/V cache element (physical page, kv head, key-in-page, dim). */
+static int64_t cache_index(const orc_problem* pb, int32_t phys, int g, int j, int d) {
+  return (((int64_t)phys * pb->num_kv_heads + g) * pb->page_size + j) * pb->head_dim + d;
+}
+
+static double dot_q_key(const orc_problem* pb, const orc_tensor* q, const orc_tensor* k,
+                        int64_t r, int32_t phys, int g, int j) {
+  const int D = pb->head_dim;
+  double s = 0.0;
+  for (int d = 0; d < D; ++d) s += elem(q, r * D + d) * elem(k, cache_index(pb, phys, g, j, d));
+  return s;
+}
+
+/* ---------------------------------------------------------------- indexer */
+
+/* scores[i][p] for rows[i] and every visible page p <= o; other entries untouched. */
+void orc_indexer(const orc_problem* pb, orc_tensor q, orc_tensor k, const int64_t* rows,
+                 int64_t nrows, double* scores, int64_t pitch) {
+  const int P = pb->page_size;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t i = 0; i < nrows; ++i) {
+    row_info ri = describe_row(pb, rows[i]);
+    for (int p = 0; p <= ri.o; ++p) {
+      int32_t phys = pb->page_table[(int64_t)ri.req * pb->max_pages + p];
+      double best = -INFINITY;
+      for (int j = 0; j < P; ++j) {
+        if ((int64_t)p * P + j > ri.t) break; /* key visible iff its position <= t */
+        double s = dot_q_key(pb, &q, &k, rows[i], phys, ri.g, j);
+        if (s > best) best = s;
+      }
+      scores[i * pitch + p] = best;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- top-k */
+
+/* idx[i][0..k) for rows[i] from scores[i][0..o]; ties (equal values, -0 == +0) go to the
+ * lower page; the own page is forced in; output ascending, padded with -1. */
+void orc_topk(const orc_problem* pb, const double* scores, int64_t pitch, const int64_t* rows,
+              int64_t nrows, int32_t* idx) {
+  const int K = pb->top_k;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < nrows; ++i) {
+    row_info ri = describe_row(pb, rows[i]);
+    int n = ri.o + 1;
+    int n_sel = n < K ? n : K;
+    char* chosen = (char*)calloc((size_t)n, 1);
+    chosen[ri.o] = 1;
+    /* n_sel - 1 passes of "best remaining other page" */
+    for (int pass = 1; pass < n_sel; ++pass) {
+      int best = -1;
+      for (int p = 0; p < n; ++p) {
+        if (chosen[p]) continue;
+        if (best < 0 || scores[i * pitch + p] > scores[i * pitch + best]) best = p;
+        /* equal values keep the earlier (lower) page because the test is strict */
+      }
+      chosen[best] = 1;
+    }
+    int w = 0;
+    for (int p = 0; p < n; ++p)
+      if (chosen[p]) idx[i * K + w++] = p;
+    for (; w < K; ++w) idx[i * K + w] = -1;
+    free(chosen);
+  }
+}
+
+/* ---------------------------------------------------------------- inversion */
+
+/* Buckets are numbered ((page_base[req] + p) * H_kv + g), page_base being the running sum of
+ * the requests' visible page counts (last own page + 1).  For each bucket, the (row, slot)
+ * pairs that selected it, in ascending row order.  Needs idx for ALL rows.  Returns the
+ * number of buckets; offsets has nbuckets + 1 entries. */
+int64_t orc_inversion(const orc_problem* pb, const int32_t* idx, int64_t* offsets,
+                      int32_t* entry_row, int32_t* entry_slot) {
+  const int K = pb->top_k, H = pb->num_q_heads, G = pb->num_kv_heads;
+  int64_t* page_base = (int64_t*)malloc(sizeof(int64_t) * (pb->batch + 1));
+  page_base[0] = 0;
+  for (int b = 0; b < pb->batch; ++b) {
+    int64_t last_t = (int64_t)pb->ctx_lens[b] + pb->q_lens[b] - 1;
+    int64_t npages = pb->q_lens[b] > 0 ? last_t / pb->page_size + 1 : 0;
+    page_base[b + 1] = page_base[b] + npages;
+  }
+  int64_t nb = page_base[pb->batch] * G;
+  int64_t T = orc_token_meta(pb, NULL, NULL);
+  int64_t R = T * H;
+  memset(offsets, 0, sizeof(int64_t) * (nb + 1));
+  /* pass 1: counts */
+  for (int64_t r = 0; r < R; ++r) {
+    row_info ri = describe_row(pb, r);
+    for (int s = 0; s < K; ++s) {
+      int p = idx[r * K + s];
+      if (p < 0) continue;
+      offsets[(page_base[ri.req] + p) * G + ri.g + 1]++;
+    }
+  }
+  for (int64_t b = 0; b < nb; ++b) offsets[b + 1] += offsets[b];
+  /* pass 2: fill in ascending row order (rows are visited in ascending order) */
+  int64_t* cursor = (int64_t*)malloc(sizeof(int64_t) * (nb > 0 ? nb : 1));
+  for (int64_t b = 0; b < nb; ++b) cursor[b] = offsets[b];
+  for (int64_t r = 0; r < R; ++r) {
+    row_info ri = describe_row(pb, r);
+    for (int s = 0; s < K; ++s) {
+      int p = idx[r * K + s];
+      if (p < 0) continue;
+      int64_t b = (page_base[ri.req] + p) * G + ri.g;
+      entry_row[cursor[b]] = (int32_t)r;
+      entry_slot[cursor[b]] = s;
+      cursor[b]++;
+    }
+  }
+  free(cursor);
+  free(page_base);
+  return nb;
+}
+
+/* ---------------------------------------------------------------- forward */
+
+/* For rows[i] and each slot s with page p = idx[i][s] >= 0: softmax over the page's visible
+ * keys of sm_scale * q.k, partial[i][s][:] = sum_j p_j v_j / l, lse[i][s] = m + ln l.
+ * Empty slots get lse = -inf and a zero partial. */
+void orc_forward(const orc_problem* pb, orc_tensor q, orc_tensor k, orc_tensor v, double sm_scale,
+                 const int32_t* idx, const int64_t* rows, int64_t nrows, double* partial,
+                 double* lse) {
+  const int P = pb->page_size, D = pb->head_dim, K = pb->top_k;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t i = 0; i < nrows; ++i) {
+    row_info ri = describe_row(pb, rows[i]);
+    double* logit = (double*)malloc(sizeof(double) * P);
+    for (int s = 0; s < K; ++s) {
+      double* out = partial + (i * K + s) * D;
+      int p = idx[i * K + s];
+      for (int d = 0; d < D; ++d) out[d] = 0.0;
+      if (p < 0) { lse[i * K + s] = -INFINITY; continue; }
+      int32_t phys = pb->page_table[(int64_t)ri.req * pb->max_pages + p];
+      int nvis = 0;
+      double m = -INFINITY;
+      for (int j = 0; j < P; ++j) {
+        if ((int64_t)p * P + j > ri.t) break; /* causal mask: only bites on the own page */
+        logit[j] = sm_scale * dot_q_key(pb, &q, &k, rows[i], phys, ri.g, j);
+        if (logit[j] > m) m = logit[j];
+        nvis = j + 1;
+      }
+      double l = 0.0;
+      for (int j = 0; j < nvis; ++j) {
+        double w = exp(logit[j] - m);
+        l += w;
+        for (int d = 0; d < D; ++d) out[d] += w * elem(&v, cache_index(pb, phys, ri.g, j, d));
+      }
+      for (int d = 0; d < D; ++d) out[d] /= l;
+      lse[i * K + s] = m + log(l);
+    }
+    free(logit);
+  }
+}
+
+/* ---------------------------------------------------------------- combine */
+
+/* out[r][:] = sum_s w_s partial_s / sum_s w_s with w_s = exp(lse_s - max lse); an empty slot
+ * (lse = -inf) is given weight 0 by selection, so whatever its partial holds cannot leak in.
+ * A row with no finite lse gets out = 0 and out_lse = -inf.  partial element (s, r, d) sits at
+ * partial[s * split_stride + r * row_stride + d]; lse (s, r) at lse[s * lse_split_stride + r]. */
+void orc_combine(int64_t rows, int32_t splits, int32_t D, const double* partial,
+                 int64_t split_stride, int64_t row_stride, const double* lse,
+                 int64_t lse_split_stride, double* out, double* out_lse) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double m = -INFINITY;
+    for (int s = 0; s < splits; ++s) {
+      double x = lse[s * lse_split_stride + r];
+      if (x > m) m = x;
+    }
+    double* o = out + r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (m == -INFINITY) { if (out_lse) out_lse[r] = -INFINITY; continue; }
+    double wsum = 0.0;
+    for (int s = 0; s < splits; ++s) {
+      double x = lse[s * lse_split_stride + r];
+      if (x == -INFINITY) continue;
+      double w = exp(x - m);
+      wsum += w;
+      const double* ps = partial + s * split_stride + r * row_stride;
+      for (int d = 0; d < D; ++d) o[d] += w * ps[d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= wsum;
+    if (out_lse) out_lse[r] = m + log(wsum);
+  }
+}
+
+/* ---------------------------------------------------------------- dense definition */
+
+/* One softmax over the union of the selected pages' visible keys, straight from the
+ * definition of block-sparse attention (no partials, no merge). */
+void orc_dense(const orc_problem* pb, orc_tensor q, orc_tensor k, orc_tensor v, double sm_scale,
+               const int32_t* idx, const int64_t* rows, int64_t nrows, double* out,
+               double* out_lse) {
+  const int P = pb->page_size, D = pb->head_dim, K = pb->top_k;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t i = 0; i < nrows; ++i) {
+    row_info ri = describe_row(pb, rows[i]);
+    int64_t cap = (int64_t)K * P;
+    double* logit = (double*)malloc(sizeof(double) * cap);
+    int32_t* kphys = (int32_t*)malloc(sizeof(int32_t) * cap);
+    int32_t* kj = (int32_t*)malloc(sizeof(int32_t) * cap);
+    int64_t n = 0;
+    double m = -INFINITY;
+    for (int s = 0; s < K; ++s) {
+      int p = idx[i * K + s];
+      if (p < 0) continue;
+      int32_t phys = pb->page_table[(int64_t)ri.req * pb->max_pages + p];
+      for (int j = 0; j < P; ++j) {
+        if ((int64_t)p * P + j > ri.t) break;
+        logit[n] = sm_scale * dot_q_key(pb, &q, &k, rows[i], phys, ri.g, j);
+        kphys[n] = phys;
+        kj[n] = j;
+        if (logit[n] > m) m = logit[n];
+        ++n;
+      }
+    }
+    double* o = out + i * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    double l = 0.0;
+    for (int64_t e = 0; e < n; ++e) {
+      double w = exp(logit[e] - m);
+      l += w;
+      for (int d = 0; d < D; ++d) o[d] += w * elem(&v, cache_index(pb, kphys[e], ri.g, kj[e], d));
+    }
+    for (int d = 0; d < D; ++d) o[d] = n ? o[d] / l : 0.0;
+    if (out_lse) out_lse[i] = n ? m + log(l) : -INFINITY;
+    free(logit);
+    free(kphys);
+    free(kj);
+  }
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
