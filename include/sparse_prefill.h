@@ -1,0 +1,243 @@
+/*
+ * sparse_prefill.h -- C ABI of the GB300 (sm_103a) paged block-sparse prefill attention
+ * library (libsps.so).
+ *
+ * The method, in four steps (terms as on the pages "MSA PR 21: Q8KV4 paged sparse prefill"
+ * and "MSA PR 36: Q8KV8 prefill indexer"):
+ *
+ *   1. indexer_scores     every causally visible 128-token KV page of every (query token,
+ *                         query head) row gets the score max_{visible keys j} q.k_j in FP32.
+ *   2. topk_select        each row keeps k pages: its own page always, the others by score
+ *                         (ties to the lower page index).
+ *   3. sparse_prefill_fwd one pass per (page, KV head, query split): each selected page yields
+ *                         a partial attention output plus its log-sum-exp (LSE), written into
+ *                         a split-strided FP32 partial buffer.  Only the row's own page is
+ *                         causally masked; K/V are read through a page table.
+ *   4. partial_combine    every row's k partials are merged by LSE into a BF16 output.
+ *
+ * Terms.  T = total query tokens of the batch (requests concatenated), H = query heads,
+ * H_kv = KV heads (H % H_kv == 0; query head h reads KV head h / (H / H_kv)), D = head_dim,
+ * page = 128 tokens.  A ROW is r = token * H + h.  Request b's token i sits at absolute
+ * position t = ctx_lens[b] + i; its own page is o = t / 128; it may see pages 0..o and, inside
+ * the own page, keys with position <= t.
+ *
+ * Memory.  The caller owns every buffer.  The library never allocates device memory; device
+ * pointers below must be device-accessible allocations on the current device.  "host" marks
+ * host pointers.  The plan (sps_plan) is an opaque host object owned by the caller.
+ *
+ * Errors.  Every call returns an sps_status.  Arguments are validated on the host first
+ * (null pointers, dtypes, 16-byte alignment where TMA reads, strides, pitches, limits); a
+ * rejected call launches nothing and returns SPS_EINVAL or SPS_EUNSUPPORTED.  A failed CUDA
+ * launch returns SPS_ECUDA.  Errors found on the device (a page-table entry out of range, a
+ * selected page the row cannot see, a bounded wait that timed out) never trap: the kernel
+ * records the first such code in a device status word and exits; read it with
+ * sps_read_device_status.  sps_last_error() gives a message for the last failing call on the
+ * calling thread.  No C++ exception crosses this interface.
+ *
+ * Streams.  All device work is asynchronous on the given stream (NULL = legacy default
+ * stream).  Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef SPARSE_PREFILL_H
+#define SPARSE_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sps_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  SPS_OK = 0,
+  SPS_EINVAL = 1,          /* bad argument (message in sps_last_error) */
+  SPS_EUNSUPPORTED = 2,    /* valid but not implemented (dtype pair, head_dim, ...) */
+  SPS_ENOSPACE = 3,        /* workspace smaller than sparse_prefill_plan asked for */
+  SPS_ECUDA = 4,           /* a CUDA runtime/driver call failed */
+  SPS_EDEVICE = 5          /* the device status word holds an error */
+} sps_status;
+
+typedef enum { SPS_BF16 = 0, SPS_FP16 = 1, SPS_E4M3 = 2, SPS_NVFP4 = 3 } sps_dtype;
+
+/* Device status codes (read with sps_read_device_status). */
+enum {
+  SPS_DEV_OK = 0,
+  SPS_DEV_TIMEOUT = 1,     /* a bounded wait gave up */
+  SPS_DEV_BAD_PAGE = 2,    /* page_table entry outside [0, num_phys_pages) */
+  SPS_DEV_BAD_INDEX = 3,   /* a selected page outside [0, own page] of its row */
+  SPS_DEV_OVERFLOW = 4     /* more work items than the plan sized the workspace for */
+};
+
+/*
+ * Problem description (host memory; copied by sparse_prefill_plan).
+ *
+ *   batch              number of requests, >= 1
+ *   q_lens, ctx_lens   host arrays [batch]: new query tokens and cached context tokens per
+ *                      request (the chunk's own K/V are already in the cache)
+ *   num_q_heads        H;  num_kv_heads: H_kv (H % H_kv == 0)
+ *   head_dim           D: 64 or 128
+ *   page_size          must be 128
+ *   top_k              k: 1..64 pages kept per row
+ *   max_pages_per_req  row length of the page table, >= every request's visible page count
+ *   num_phys_pages     number of physical pages in the K/V caches
+ *   q_dtype / kv_dtype           attention inputs: BF16/BF16 or E4M3/NVFP4
+ *   idx_q_dtype / idx_k_dtype    indexer inputs: BF16/BF16, E4M3/E4M3 or E4M3/NVFP4
+ *   softmax_scale      multiplier of q.k inside the softmax (typically 1/sqrt(D))
+ */
+typedef struct {
+  int32_t batch;
+  const int32_t* q_lens;
+  const int32_t* ctx_lens;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t top_k;
+  int32_t max_pages_per_req;
+  int32_t num_phys_pages;
+  sps_dtype q_dtype;
+  sps_dtype kv_dtype;
+  sps_dtype idx_q_dtype;
+  sps_dtype idx_k_dtype;
+  float softmax_scale;
+} sps_problem;
+
+typedef struct sps_plan sps_plan;
+
+/* Sizes and workspace offsets of a plan (for inspection and tests).  Offsets are bytes from
+ * the workspace base. */
+typedef struct {
+  int64_t num_tokens;        /* T */
+  int64_t num_rows;          /* T * H */
+  int64_t num_buckets;       /* (request, visible page, KV head) triples */
+  int64_t max_entries;       /* num_rows * top_k */
+  int64_t indexer_tasks;     /* indexer work items */
+  int64_t max_fwd_tasks;     /* upper bound on forward work items */
+  int64_t workspace_bytes;
+  int64_t off_status;        /* int32 device status word */
+  int64_t off_tok_pos;       /* int32 [T]: absolute position of each token */
+  int64_t off_tok_req;       /* int32 [T]: request of each token */
+  int64_t off_bucket_offsets;/* int32 [num_buckets + 1]: CSR offsets of the inversion */
+  int64_t off_entries;       /* int32 pairs [max_entries]: (row, slot), rows ascending per bucket */
+  int64_t off_fwd_task_count;/* int32: number of forward work items built on the device */
+} sps_plan_info;
+
+/*
+ * sparse_prefill_plan -- host only, no device work.
+ * Validates the problem, derives per-token metadata, the indexer's work list (query tile x
+ * page chunk; the chunk shrinks from 128 to 8 pages until the work fills the GPU, as the
+ * adaptive page chunk of "MSA PR 36", Changes) and the workspace layout (one workspace may
+ * serve every call of this plan in order on one stream, as the PrefillWorkspace of "MSA PR
+ * 21", Place the partials by memory locality domain).
+ *   plan            out: new plan, free with sps_plan_destroy
+ *   workspace_bytes out: device workspace size the plan's calls need (256-byte aligned)
+ * Returns SPS_EINVAL / SPS_EUNSUPPORTED for a problem it cannot run.
+ */
+sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** plan,
+                               size_t* workspace_bytes);
+
+void sps_plan_destroy(sps_plan* plan);
+
+sps_status sps_plan_get_info(const sps_plan* plan, sps_plan_info* info);
+
+/*
+ * sps_plan_upload -- copies the plan's metadata into `workspace` (device, >= workspace_bytes,
+ * 256-byte aligned) on `stream` and clears the device status word.  Call once per (plan,
+ * workspace) before the other plan calls, on the same stream.  The plan must stay alive
+ * until the copy has completed (the copy reads the plan's pinned host buffer).
+ */
+sps_status sps_plan_upload(const sps_plan* plan, void* workspace, size_t workspace_bytes,
+                           sps_stream_t stream);
+
+/*
+ * indexer_scores -- step 1 ("MSA PR 36", Changes: per-page max by TMEM load-and-reduce;
+ * Wrapper API: caller-owned score buffer).
+ *   q_idx        device [T][H][D] in idx_q_dtype (E4M3: one byte per element)
+ *   q_scale      per-tensor multiplier of the decoded q (1 for BF16)
+ *   k_idx_cache  device [num_phys_pages][H_kv][128][D] in idx_k_dtype; NVFP4: packed codes
+ *                [..][128][D/2], the even element in the low nibble
+ *   k_idx_scales device [num_phys_pages][H_kv][128][D/16] E4M3 (NVFP4 only, else NULL)
+ *   k_scale      per-tensor multiplier of the decoded k (1 for BF16 and NVFP4)
+ *   page_table   device int32 [batch][max_pages_per_req], logical -> physical page
+ *   scores       device FP32 [T*H][score_pitch]; score_pitch >= max_pages_per_req, 4-aligned
+ * Writes scores[r][p] = q_scale * k_scale * max_{j in page p, j <= t} (q_r . k_j) for every
+ * p <= o(r); every other entry is left untouched.  Accumulation is FP32.
+ */
+sps_status indexer_scores(const sps_plan* plan, const void* q_idx, float q_scale,
+                          const void* k_idx_cache, const void* k_idx_scales, float k_scale,
+                          const int32_t* page_table, float* scores, int64_t score_pitch,
+                          void* workspace, sps_stream_t stream);
+
+/*
+ * topk_select -- step 2 (north-star definition; bitwise-stable selection, "MSA PR 36",
+ * Kernel performance table: top-k bitwise identical).
+ *   scores  device FP32 [T*H][score_pitch] as written by indexer_scores (entries p <= o read)
+ *   idx     device int32 [T*H][top_k] out: the selected pages of each row in ascending page
+ *           order, padded with -1 when the row sees fewer than top_k pages.
+ * The own page o is always kept; the other min(top_k, o+1) - 1 are the best by (score
+ * descending, page ascending), with -0.0 equal to +0.0.  NaN scores are outside the contract.
+ */
+sps_status topk_select(const sps_plan* plan, const float* scores, int64_t score_pitch,
+                       int32_t* idx, void* workspace, sps_stream_t stream);
+
+/*
+ * sparse_prefill_fwd -- step 3 ("MSA PR 21", K1: one CTA per (page, head, query split),
+ * groups of 128 query rows, own-page-only causal mask; K1 also reads the split stride).
+ *   q            device [T][H][D], q_dtype (BF16, or E4M3 with q_scale)
+ *   k_cache, v_cache  device [num_phys_pages][H_kv][128][D] (BF16), or NVFP4 codes
+ *                [..][128][D/2] with k_scales / v_scales [..][128][D/16] E4M3
+ *   page_table   device int32 [batch][max_pages_per_req]
+ *   idx          device int32 [T*H][top_k] from topk_select (or any selection obeying its
+ *                contract: ascending, -1 padded, pages <= own page)
+ *   partial      device FP32; element (slot s, row r, dim d) at
+ *                partial[s * split_stride + r * D + d]; split_stride >= T*H*D, multiple of 4
+ *   lse          device FP32; (s, r) at lse[s * lse_split_stride + r]; stride >= T*H
+ * For every row r and slot s with page p = idx[r][s] >= 0: the softmax over the page's keys
+ * j <= t of softmax_scale * q.k_j gives partial = sum_j p_j v_j / l (FP32) and
+ * lse = m + ln(l) (natural log).  Empty slots (idx = -1) get lse = -inf and their partial is
+ * not written.  P is rounded to FP16 for the P.V product; V is converted to FP16 (exact for
+ * NVFP4 and for BF16 values in the FP16 normal range).
+ */
+sps_status sparse_prefill_fwd(const sps_plan* plan, const void* q, float q_scale,
+                              const void* k_cache, const void* v_cache, const void* k_scales,
+                              const void* v_scales, const int32_t* page_table,
+                              const int32_t* idx, float* partial, int64_t split_stride,
+                              float* lse, int64_t lse_split_stride, void* workspace,
+                              sps_stream_t stream);
+
+/*
+ * partial_combine -- step 4 ("MSA PR 21", Combine: one streaming kernel; a CTA owns
+ * consecutive rows, the splits stream through a shared-memory ring of bulk copies).
+ * Plan-free so it can run on any partial buffer.
+ *   rows, splits, head_dim  R, S (1..64), D (64 or 128)
+ *   partial   device FP32, (s, r, d) at partial[s * split_stride + r * head_dim + d];
+ *             16-byte aligned, split_stride a multiple of 4 and >= rows * head_dim
+ *   lse       device FP32, (s, r) at lse[s * lse_split_stride + r], lse_split_stride >= rows
+ *   out_bf16  device BF16, row r at out_bf16 + r * out_row_stride (elements); 16-byte aligned,
+ *             out_row_stride a multiple of 8
+ *   out_lse   device FP32 [rows] or NULL
+ *   dev_status device int32 status word or NULL (a wait that times out records there)
+ * out[r] = sum_s w_s partial_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s); a slot with
+ * lse = -inf gets weight 0 by selection (its partial is never read); a row whose slots are
+ * all -inf gets out = 0 and out_lse = -inf.  FP32 accumulation, BF16 round-to-nearest output.
+ */
+sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const float* partial,
+                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                           void* out_bf16, int64_t out_row_stride, float* out_lse,
+                           int32_t* dev_status, sps_stream_t stream);
+
+/*
+ * sps_read_device_status -- synchronous: waits for the device, then copies the plan
+ * workspace's status word into *code (SPS_DEV_*).  Returns SPS_EDEVICE when it is non-zero.
+ */
+sps_status sps_read_device_status(const sps_plan* plan, const void* workspace, int32_t* code);
+
+/* Message of the last failing call on the calling thread ("" if none). */
+const char* sps_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_PREFILL_H */

@@ -1,0 +1,519 @@
+// host.cpp -- C ABI of libsps: problem validation, the plan (per-token metadata, indexer work
+// list, workspace layout), the metadata upload, and the argument checks in front of every
+// kernel launch.  No device memory is ever allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "sps_internal.h"
+
+using namespace sps;
+
+namespace {
+
+thread_local std::string g_err;
+
+sps_status fail(sps_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+sps_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SPS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+}  // namespace
+
+struct sps_plan {
+  sps_problem pb;                 // copy (host arrays below)
+  std::vector<int32_t> q_lens, ctx_lens;
+  std::vector<ReqInfo> reqs;
+  std::vector<int32_t> page_req;  // [total_pages]
+  std::vector<IdxTask> idx_tasks;
+  int64_t T = 0, R = 0, num_buckets = 0, max_entries = 0, max_fwd_tasks = 0;
+  int64_t total_pages = 0, bm_total_words = 0;
+  // workspace layout (bytes)
+  int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
+          off_page_req = 0, off_idx_tasks = 0, off_bitmap = 0, off_bucket_count = 0,
+          off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
+  int64_t upload_bytes = 0;  // [off_tok_pos, off_tok_pos + upload_bytes) comes from `blob`
+  std::vector<uint8_t> blob;
+};
+
+namespace {
+
+sps_status validate_problem(const sps_problem* p) {
+  if (!p) return fail(SPS_EINVAL, "problem is NULL");
+  if (p->batch < 1) return fail(SPS_EINVAL, "batch must be >= 1 (got %d)", p->batch);
+  if (!p->q_lens || !p->ctx_lens) return fail(SPS_EINVAL, "q_lens/ctx_lens must be host arrays");
+  if (p->page_size != kPage) return fail(SPS_EUNSUPPORTED, "page_size must be 128");
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return fail(SPS_EUNSUPPORTED, "head_dim must be 64 or 128 (got %d)", p->head_dim);
+  if (p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_q_heads % p->num_kv_heads)
+    return fail(SPS_EINVAL, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                p->num_q_heads, p->num_kv_heads);
+  if (p->top_k < 1 || p->top_k > kMaxTopK)
+    return fail(SPS_EINVAL, "top_k must be in [1, %d] (got %d)", kMaxTopK, p->top_k);
+  if (p->num_phys_pages < 1) return fail(SPS_EINVAL, "num_phys_pages must be >= 1");
+  if (!(p->softmax_scale > 0.f) || !std::isfinite(p->softmax_scale))
+    return fail(SPS_EINVAL, "softmax_scale must be finite and > 0");
+  bool attn_ok = (p->q_dtype == SPS_BF16 && p->kv_dtype == SPS_BF16) ||
+                 (p->q_dtype == SPS_E4M3 && p->kv_dtype == SPS_NVFP4);
+  if (!attn_ok) return fail(SPS_EUNSUPPORTED, "attention dtypes must be BF16/BF16 or E4M3/NVFP4");
+  bool idx_ok = (p->idx_q_dtype == SPS_BF16 && p->idx_k_dtype == SPS_BF16) ||
+                (p->idx_q_dtype == SPS_E4M3 && p->idx_k_dtype == SPS_E4M3) ||
+                (p->idx_q_dtype == SPS_E4M3 && p->idx_k_dtype == SPS_NVFP4);
+  if (!idx_ok)
+    return fail(SPS_EUNSUPPORTED, "indexer dtypes must be BF16/BF16, E4M3/E4M3 or E4M3/NVFP4");
+  int64_t T = 0;
+  for (int b = 0; b < p->batch; ++b) {
+    if (p->q_lens[b] < 0 || p->ctx_lens[b] < 0)
+      return fail(SPS_EINVAL, "request %d: negative q_len/ctx_len", b);
+    int64_t last = (int64_t)p->ctx_lens[b] + p->q_lens[b] - 1;
+    if (last >= (int64_t)1 << 30) return fail(SPS_EINVAL, "request %d: sequence too long", b);
+    int64_t np = p->q_lens[b] > 0 ? last / kPage + 1 : 0;
+    if (np > p->max_pages_per_req)
+      return fail(SPS_EINVAL, "request %d needs %lld pages > max_pages_per_req %d", b,
+                  (long long)np, p->max_pages_per_req);
+    T += p->q_lens[b];
+  }
+  if (T < 1) return fail(SPS_EINVAL, "the batch has no query tokens");
+  int64_t R = T * p->num_q_heads;
+  if (R * p->top_k >= ((int64_t)1 << 31) || R * p->head_dim >= ((int64_t)1 << 40))
+    return fail(SPS_EUNSUPPORTED, "batch too large (rows x top_k must stay below 2^31)");
+  if (p->max_pages_per_req > 512)
+    return fail(SPS_EUNSUPPORTED, "max_pages_per_req above 512 (64K tokens) is not supported");
+  return SPS_OK;
+}
+
+// Indexer work list: tiles of <= 128 tokens x (1 or 2 heads of one KV group) against page
+// chunks; the chunk starts at 128 pages and halves (down to 8) until there are enough items
+// for a few waves.  Items are ordered by decreasing page count (largest first), then by
+// their natural order, so a static round-robin over CTAs balances well.
+void build_indexer_tasks(sps_plan* pl) {
+  const sps_problem& p = pl->pb;
+  const int Hg = p.num_q_heads / p.num_kv_heads;
+  const int nh = (Hg % 2 == 0) ? 2 : 1;
+  const int64_t target = 4LL * std::max(1, num_sms());
+  int chunk = 128;
+  for (;;) {
+    std::vector<IdxTask> tasks;
+    for (int b = 0; b < p.batch; ++b) {
+      const ReqInfo& ri = pl->reqs[b];
+      for (int i0 = 0; i0 < ri.q_len; i0 += kPage) {
+        int ntok = std::min(kPage, ri.q_len - i0);
+        int o_last = (ri.ctx + i0 + ntok - 1) / kPage;
+        for (int g = 0; g < p.num_kv_heads; ++g)
+          for (int hl = 0; hl < Hg; hl += nh)
+            for (int pb = 0; pb <= o_last; pb += chunk) {
+              IdxTask t;
+              t.req = b;
+              t.g = g;
+              t.h0 = g * Hg + hl;
+              t.nh = nh;
+              t.tok0 = ri.tok0 + i0;
+              t.ntok = ntok;
+              t.page_begin = pb;
+              t.page_end = std::min(o_last + 1, pb + chunk);
+              tasks.push_back(t);
+            }
+      }
+    }
+    if ((int64_t)tasks.size() >= target || chunk <= 8) {
+      std::stable_sort(tasks.begin(), tasks.end(), [](const IdxTask& a, const IdxTask& b) {
+        return (a.page_end - a.page_begin) > (b.page_end - b.page_begin);
+      });
+      pl->idx_tasks.swap(tasks);
+      return;
+    }
+    chunk /= 2;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sps_last_error(void) { return g_err.c_str(); }
+
+sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
+                               size_t* workspace_bytes) {
+  if (!out || !workspace_bytes) return fail(SPS_EINVAL, "plan/workspace_bytes out-pointers NULL");
+  *out = nullptr;
+  sps_status st = validate_problem(problem);
+  if (st != SPS_OK) return st;
+  sps_plan* pl = new (std::nothrow) sps_plan();
+  if (!pl) return fail(SPS_EINVAL, "out of host memory");
+  pl->pb = *problem;
+  const sps_problem& p = pl->pb;
+  pl->q_lens.assign(problem->q_lens, problem->q_lens + p.batch);
+  pl->ctx_lens.assign(problem->ctx_lens, problem->ctx_lens + p.batch);
+  pl->pb.q_lens = pl->q_lens.data();
+  pl->pb.ctx_lens = pl->ctx_lens.data();
+  const int Hg = p.num_q_heads / p.num_kv_heads;
+
+  // per-request info, per-token metadata
+  std::vector<int32_t> tok_pos, tok_req;
+  int32_t tok = 0, page_base = 0, bm_base = 0;
+  for (int b = 0; b < p.batch; ++b) {
+    ReqInfo ri{};
+    ri.tok0 = tok;
+    ri.q_len = pl->q_lens[b];
+    ri.ctx = pl->ctx_lens[b];
+    ri.npages = ri.q_len > 0 ? (ri.ctx + ri.q_len - 1) / kPage + 1 : 0;
+    ri.page_base = page_base;
+    ri.bm_words = (int32_t)((int64_t(ri.q_len) * Hg + 31) / 32);
+    ri.bm_base = bm_base;
+    for (int i = 0; i < ri.q_len; ++i) {
+      tok_pos.push_back(ri.ctx + i);
+      tok_req.push_back(b);
+    }
+    for (int pg = 0; pg < ri.npages; ++pg) pl->page_req.push_back(b);
+    bm_base += ri.npages * p.num_kv_heads * ri.bm_words;
+    page_base += ri.npages;
+    tok += ri.q_len;
+    pl->reqs.push_back(ri);
+  }
+  pl->T = tok;
+  pl->R = (int64_t)tok * p.num_q_heads;
+  pl->total_pages = page_base;
+  pl->num_buckets = (int64_t)page_base * p.num_kv_heads;
+  pl->bm_total_words = bm_base;
+  pl->max_entries = pl->R * p.top_k;
+  const int64_t per_task = (int64_t)kFwdTaskGroups * 128;
+  pl->max_fwd_tasks = pl->max_entries / per_task + pl->num_buckets + 1;
+  build_indexer_tasks(pl);
+
+  // workspace layout
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    int64_t o = off;
+    off = align_up(off + std::max<int64_t>(bytes, 4), 256);
+    return o;
+  };
+  pl->off_status = take(4);
+  pl->off_counters = take(16 * 4);
+  pl->off_tok_pos = take(4 * pl->T);
+  pl->off_tok_req = take(4 * pl->T);
+  pl->off_reqs = take(sizeof(ReqInfo) * p.batch);
+  pl->off_page_req = take(4 * std::max<int64_t>(1, pl->total_pages));
+  pl->off_idx_tasks = take(sizeof(IdxTask) * std::max<size_t>(1, pl->idx_tasks.size()));
+  int64_t upload_end = off;
+  pl->off_bitmap = take(4 * std::max<int64_t>(1, pl->bm_total_words));
+  pl->off_bucket_count = take(4 * std::max<int64_t>(1, pl->num_buckets));
+  pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
+  pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
+  pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
+  pl->ws_bytes = off;
+
+  // the host image of [off_tok_pos, upload_end)
+  pl->upload_bytes = upload_end - pl->off_tok_pos;
+  pl->blob.assign(pl->upload_bytes, 0);
+  auto put = [&](int64_t o, const void* src, size_t n) {
+    if (n) memcpy(pl->blob.data() + (o - pl->off_tok_pos), src, n);
+  };
+  put(pl->off_tok_pos, tok_pos.data(), 4 * tok_pos.size());
+  put(pl->off_tok_req, tok_req.data(), 4 * tok_req.size());
+  put(pl->off_reqs, pl->reqs.data(), sizeof(ReqInfo) * pl->reqs.size());
+  put(pl->off_page_req, pl->page_req.data(), 4 * pl->page_req.size());
+  put(pl->off_idx_tasks, pl->idx_tasks.data(), sizeof(IdxTask) * pl->idx_tasks.size());
+
+  *out = pl;
+  *workspace_bytes = (size_t)pl->ws_bytes;
+  return SPS_OK;
+}
+
+void sps_plan_destroy(sps_plan* plan) { delete plan; }
+
+sps_status sps_plan_get_info(const sps_plan* pl, sps_plan_info* info) {
+  if (!pl || !info) return fail(SPS_EINVAL, "plan/info NULL");
+  info->num_tokens = pl->T;
+  info->num_rows = pl->R;
+  info->num_buckets = pl->num_buckets;
+  info->max_entries = pl->max_entries;
+  info->indexer_tasks = (int64_t)pl->idx_tasks.size();
+  info->max_fwd_tasks = pl->max_fwd_tasks;
+  info->workspace_bytes = pl->ws_bytes;
+  info->off_status = pl->off_status;
+  info->off_tok_pos = pl->off_tok_pos;
+  info->off_tok_req = pl->off_tok_req;
+  info->off_bucket_offsets = pl->off_bucket_offsets;
+  info->off_entries = pl->off_entries;
+  info->off_fwd_task_count = pl->off_counters + 2 * 4;
+  return SPS_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const sps_problem& p = pl->pb;
+  DevPlan d{};
+  d.batch = p.batch;
+  d.T = (int32_t)pl->T;
+  d.H = p.num_q_heads;
+  d.Hkv = p.num_kv_heads;
+  d.Hg = p.num_q_heads / p.num_kv_heads;
+  d.D = p.head_dim;
+  d.K = p.top_k;
+  d.max_pages = p.max_pages_per_req;
+  d.num_phys = p.num_phys_pages;
+  d.num_buckets = (int32_t)pl->num_buckets;
+  d.max_entries = (int32_t)pl->max_entries;
+  d.max_fwd_tasks = (int32_t)pl->max_fwd_tasks;
+  d.n_idx_tasks = (int32_t)pl->idx_tasks.size();
+  d.total_pages = (int32_t)pl->total_pages;
+  d.bm_total_words = (int32_t)pl->bm_total_words;
+  d.mark_warps = 0;
+  for (const ReqInfo& ri : pl->reqs) d.mark_warps += (int64_t)p.num_kv_heads * ri.bm_words;
+  d.sm_scale = p.softmax_scale;
+  d.status = reinterpret_cast<int32_t*>(base + pl->off_status);
+  d.counters = reinterpret_cast<int32_t*>(base + pl->off_counters);
+  d.tok_pos = reinterpret_cast<const int32_t*>(base + pl->off_tok_pos);
+  d.tok_req = reinterpret_cast<const int32_t*>(base + pl->off_tok_req);
+  d.reqs = reinterpret_cast<const ReqInfo*>(base + pl->off_reqs);
+  d.page_req = reinterpret_cast<const int32_t*>(base + pl->off_page_req);
+  d.idx_tasks = reinterpret_cast<const IdxTask*>(base + pl->off_idx_tasks);
+  d.bitmap = reinterpret_cast<uint32_t*>(base + pl->off_bitmap);
+  d.bucket_count = reinterpret_cast<int32_t*>(base + pl->off_bucket_count);
+  d.bucket_offsets = reinterpret_cast<int32_t*>(base + pl->off_bucket_offsets);
+  d.entries = reinterpret_cast<int2*>(base + pl->off_entries);
+  d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
+  return d;
+}
+
+sps_status check_plan_ws(const sps_plan* pl, const void* ws) {
+  if (!pl) return fail(SPS_EINVAL, "plan is NULL");
+  if (!ws) return fail(SPS_EINVAL, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(SPS_EINVAL, "workspace must be 256-byte aligned");
+  return SPS_OK;
+}
+
+sps_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return SPS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sps_status sps_plan_upload(const sps_plan* pl, void* ws, size_t ws_bytes, sps_stream_t stream) {
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  if ((int64_t)ws_bytes < pl->ws_bytes)
+    return fail(SPS_ENOSPACE, "workspace of %zu bytes < %lld required", ws_bytes,
+                (long long)pl->ws_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);  // status + counters
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  e = cudaMemcpyAsync(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes,
+                      cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan upload)");
+  return SPS_OK;
+}
+
+sps_status indexer_scores(const sps_plan* pl, const void* q_idx, float q_scale,
+                          const void* k_idx_cache, const void* k_idx_scales, float k_scale,
+                          const int32_t* page_table, float* scores, int64_t score_pitch,
+                          void* ws, sps_stream_t stream) {
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  const sps_problem& p = pl->pb;
+  if (!q_idx || !k_idx_cache || !page_table || !scores)
+    return fail(SPS_EINVAL, "indexer_scores: NULL input/output pointer");
+  if (p.idx_k_dtype == SPS_NVFP4 && !k_idx_scales)
+    return fail(SPS_EINVAL, "indexer_scores: NVFP4 keys need k_idx_scales");
+  if (score_pitch < p.max_pages_per_req)
+    return fail(SPS_EINVAL, "score_pitch %lld < max_pages_per_req %d", (long long)score_pitch,
+                p.max_pages_per_req);
+  if (!aligned(q_idx, 16) || !aligned(k_idx_cache, 16) || (k_idx_scales && !aligned(k_idx_scales, 16)))
+    return fail(SPS_EINVAL, "indexer_scores: q/k buffers must be 16-byte aligned");
+  if (!aligned(scores, 4)) return fail(SPS_EINVAL, "scores must be 4-byte aligned");
+  if (!std::isfinite(q_scale) || !std::isfinite(k_scale))
+    return fail(SPS_EINVAL, "indexer_scores: scales must be finite");
+  DevPlan d = make_dev_plan(pl, ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return launched(launch_indexer(d, p.idx_q_dtype, p.idx_k_dtype, q_idx, q_scale, k_idx_cache,
+                                 k_idx_scales, k_scale, page_table, scores, score_pitch, s),
+                  "indexer launch");
+}
+
+sps_status topk_select(const sps_plan* pl, const float* scores, int64_t score_pitch,
+                       int32_t* idx, void* ws, sps_stream_t stream) {
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  if (!scores || !idx) return fail(SPS_EINVAL, "topk_select: NULL scores/idx");
+  if (score_pitch < pl->pb.max_pages_per_req)
+    return fail(SPS_EINVAL, "score_pitch %lld < max_pages_per_req %d", (long long)score_pitch,
+                pl->pb.max_pages_per_req);
+  if (!aligned(scores, 4) || !aligned(idx, 4)) return fail(SPS_EINVAL, "misaligned scores/idx");
+  DevPlan d = make_dev_plan(pl, ws);
+  return launched(launch_topk(d, scores, score_pitch, idx, reinterpret_cast<cudaStream_t>(stream)),
+                  "top-k launch");
+}
+
+sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
+                              const void* k_cache, const void* v_cache, const void* k_scales,
+                              const void* v_scales, const int32_t* page_table,
+                              const int32_t* idx, float* partial, int64_t split_stride,
+                              float* lse, int64_t lse_split_stride, void* ws,
+                              sps_stream_t stream) {
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  const sps_problem& p = pl->pb;
+  if (!q || !k_cache || !v_cache || !page_table || !idx || !partial || !lse)
+    return fail(SPS_EINVAL, "sparse_prefill_fwd: NULL input/output pointer");
+  if (p.kv_dtype == SPS_NVFP4 && (!k_scales || !v_scales))
+    return fail(SPS_EINVAL, "sparse_prefill_fwd: NVFP4 K/V need k_scales and v_scales");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      (k_scales && !aligned(k_scales, 16)) || (v_scales && !aligned(v_scales, 16)))
+    return fail(SPS_EINVAL, "sparse_prefill_fwd: q/k/v buffers must be 16-byte aligned");
+  if (!aligned(partial, 16)) return fail(SPS_EINVAL, "partial must be 16-byte aligned");
+  if (split_stride < pl->R * p.head_dim || split_stride % 4)
+    return fail(SPS_EINVAL, "split_stride must be >= rows*head_dim and a multiple of 4");
+  if (lse_split_stride < pl->R) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
+  if (!std::isfinite(q_scale)) return fail(SPS_EINVAL, "q_scale must be finite");
+  DevPlan d = make_dev_plan(pl, ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // counters [1] (forward task cursor) and [2] (task count) start at zero
+  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+  e = launch_inversion(d, idx, lse, lse_split_stride, s);
+  if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
+  return launched(launch_forward(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache, k_scales,
+                                 v_scales, page_table, partial, split_stride, lse,
+                                 lse_split_stride, s),
+                  "forward launch");
+}
+
+sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const float* partial,
+                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                           void* out_bf16, int64_t out_row_stride, float* out_lse,
+                           int32_t* dev_status, sps_stream_t stream) {
+  if (rows < 0) return fail(SPS_EINVAL, "rows must be >= 0");
+  if (splits < 1 || splits > kMaxTopK) return fail(SPS_EINVAL, "splits must be in [1, 64]");
+  if (head_dim != 64 && head_dim != 128) return fail(SPS_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (rows == 0) return SPS_OK;
+  if (!partial || !lse || !out_bf16) return fail(SPS_EINVAL, "partial_combine: NULL pointer");
+  if (!aligned(partial, 16) || !aligned(out_bf16, 16) || !aligned(lse, 4))
+    return fail(SPS_EINVAL, "partial/out must be 16-byte aligned, lse 4-byte aligned");
+  if (split_stride % 4 || split_stride < rows * head_dim)
+    return fail(SPS_EINVAL, "split_stride must be a multiple of 4 and >= rows*head_dim");
+  if (lse_split_stride < rows) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
+  if (out_row_stride < head_dim || out_row_stride % 8)
+    return fail(SPS_EINVAL, "out_row_stride must be >= head_dim and a multiple of 8");
+  return launched(launch_combine(rows, splits, head_dim, partial, split_stride, lse,
+                                 lse_split_stride, out_bf16, out_row_stride, out_lse, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream)),
+                  "combine launch");
+}
+
+sps_status sps_read_device_status(const sps_plan* pl, const void* ws, int32_t* code) {
+  if (!code) return fail(SPS_EINVAL, "code is NULL");
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(code, static_cast<const uint8_t*>(ws) + pl->off_status, 4,
+                 cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (*code != 0) return fail(SPS_EDEVICE, "device status %d", *code);
+  return SPS_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ driver helpers
+namespace sps {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+void load_encode() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+CUtensorMapDataType tm_type(int code) {
+  switch (code) {
+    case 0: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case 1: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  }
+}
+int tm_size(int code) { return code <= 1 ? 2 : 1; }
+}  // namespace
+
+bool encode_tmap_2d(void* map, int dtype_code, void* base, uint64_t inner, uint64_t outer,
+                    uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {outer_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  (void)tm_size;
+  return g_encode(reinterpret_cast<CUtensorMap*>(map), tm_type(dtype_code), 2, base, dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d(void* map, int dtype_code, void* base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1,
+                    uint32_t b2, bool swizzle128) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(reinterpret_cast<CUtensorMap*>(map), tm_type(dtype_code), 3, base, dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = -1;
+  if (n < 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 152;  // planning without a device: the GB300 SM count
+  }
+  return n;
+}
+
+}  // namespace sps

@@ -1,0 +1,87 @@
+// sps_internal.h -- plan layout shared by the host library and the kernels (not installed).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/sparse_prefill.h"
+
+namespace sps {
+
+constexpr int kPage = 128;         // tokens per KV page
+constexpr int kMaxTopK = 64;
+constexpr int kFwdTaskGroups = 8;  // 128-row query groups per forward work item
+
+// One request of the batch, as the kernels see it.
+struct ReqInfo {
+  int32_t tok0;       // first flat token of the request
+  int32_t q_len;      // new tokens
+  int32_t ctx;        // cached tokens before them
+  int32_t npages;     // visible pages of the request's last token (own page + 1)
+  int32_t page_base;  // running sum of npages over earlier requests
+  int32_t bm_base;    // first selection-bitmap word of the request
+  int32_t bm_words;   // words per (page, KV head) bucket: ceil(q_len * H/H_kv / 32)
+  int32_t pad;
+};
+
+// Indexer work item: query tile (<=128 tokens of one request, 1-2 query heads of one KV
+// group) against the page chunk [page_begin, page_end).
+struct IdxTask {
+  int32_t req, g, h0, nh;
+  int32_t tok0, ntok, page_begin, page_end;
+};
+
+// Forward work item: up to kFwdTaskGroups x 128 entries of one (request, page, KV head)
+// bucket, entries [entry_begin, entry_begin + count).
+struct FwdTask {
+  int32_t bucket, entry_begin, count, pad;
+};
+
+// Everything a kernel needs about the plan, passed by value.
+struct DevPlan {
+  int32_t batch, T, H, Hkv, Hg, D, K, max_pages, num_phys;
+  int32_t num_buckets, max_entries, max_fwd_tasks, n_idx_tasks, total_pages, bm_total_words;
+  int64_t mark_warps;       // sum over requests of H_kv * bm_words (one warp per bitmap word)
+  float sm_scale;
+  int32_t* status;
+  int32_t* counters;        // [0] indexer task cursor, [1] forward task cursor, [2] fwd task count
+  const int32_t* tok_pos;   // [T]
+  const int32_t* tok_req;   // [T]
+  const ReqInfo* reqs;      // [batch]
+  const int32_t* page_req;  // [total_pages]: request of each global page slot
+  const IdxTask* idx_tasks; // [n_idx_tasks]
+  uint32_t* bitmap;         // [bm_total_words]
+  int32_t* bucket_count;    // [num_buckets]
+  int32_t* bucket_offsets;  // [num_buckets + 1]
+  int2* entries;            // [max_entries] (row, slot)
+  FwdTask* fwd_tasks;       // [max_fwd_tasks]
+};
+
+// Launchers (one per kernel file).  Return cudaSuccess or the launch error.
+cudaError_t launch_combine(int64_t rows, int32_t splits, int32_t D, const float* partial,
+                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                           void* out, int64_t out_row_stride, float* out_lse, int32_t* status,
+                           cudaStream_t st);
+cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, int32_t* idx,
+                        cudaStream_t st);
+cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
+                             int64_t lse_split_stride, cudaStream_t st);
+cudaError_t launch_indexer(const DevPlan& p, sps_dtype qt, sps_dtype kt, const void* q,
+                           float q_scale, const void* kc, const void* kscales, float k_scale,
+                           const int32_t* page_table, float* scores, int64_t pitch,
+                           cudaStream_t st);
+cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                           float q_scale, const void* kc, const void* vc, const void* ks,
+                           const void* vs, const int32_t* page_table, float* partial,
+                           int64_t split_stride, float* lse, int64_t lse_split_stride,
+                           cudaStream_t st);
+
+// Tensor-map encoding through the driver entry point (no link against libcuda).
+bool encode_tmap_2d(void* map, int dtype_code, void* base, uint64_t inner, uint64_t outer,
+                    uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128);
+bool encode_tmap_3d(void* map, int dtype_code, void* base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1,
+                    uint32_t b2, bool swizzle128);
+int num_sms();
+
+}  // namespace sps

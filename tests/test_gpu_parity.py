@@ -1,0 +1,297 @@
+"""GPU parity: every step through the C ABI against the FP64 oracle on the same seeded inputs.
+
+Tolerances (the method's stated bar):
+  * plan metadata, page selection and the page -> row inversion: bit-exact;
+  * scores: |s_gpu - s_ref| <= 1e-5 * max(|s_ref|, A), A = max over the page's visible keys of
+    sum_i |q_i k_ji| (the second term covers near-cancelling dot products);
+  * partials: relative L2 <= 1e-3 per checked set, LSE: abs <= 1e-4;
+  * output: relative L2 <= 2e-3 and max abs <= 1e-2 for BF16 inputs, 5e-3 / 2e-2 for
+    E4M3/NVFP4 inputs (against the oracle on the dequantised values).
+Top-k is checked on the shared GPU score buffer and the forward on the shared GPU selection,
+so each step is compared on identical inputs.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import oracle as orc
+from paged_top_sparse_gb300 import synth
+from tests.helpers import oracle_problem, oracle_tensors, rel_l2, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+SCORE_RTOL = 1e-5
+PARTIAL_RL2 = 1e-3
+LSE_ATOL = 1e-4
+OUT_TOL = {"bf16": (2e-3, 1e-2), "quant": (5e-3, 2e-2)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_top_sparse_gb300 import build
+
+    build.build()
+
+
+def _workload(name):
+    if name == "ragged":
+        return synth.workload("custom", seed=11, q_lens=[300, 77, 129], ctx_lens=[0, 1000, 250],
+                              num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=5)
+    if name == "mha_d64":
+        return synth.workload("custom", seed=12, q_lens=[200], ctx_lens=[130], num_q_heads=3,
+                              num_kv_heads=3, head_dim=64, top_k=2)
+    if name == "k1":
+        return synth.workload("custom", seed=13, q_lens=[257], ctx_lens=[0], num_q_heads=2,
+                              num_kv_heads=1, head_dim=128, top_k=1)
+    return synth.workload(name, seed=0)
+
+
+SMALL = ["tiny", "ragged", "mha_d64", "k1"]
+_cache = {}
+
+
+def _run(name):
+    """Run the whole path once per workload (module cache) and return everything."""
+    if name in _cache:
+        return _cache[name]
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload(name)
+    t = synth.make_tensors(w)
+    run = DeviceRun(w, t)
+    run.run_all()
+    assert run.status() == 0
+    full = w.num_rows <= 20000
+    rows = np.arange(w.num_rows, dtype=np.int64) if full else sample_rows(w, 384)
+    rows_t = torch.from_numpy(rows).to(run.dev)
+    res = dict(
+        w=w, t=t, run=run, rows=rows,
+        scores=run.scores[rows_t].cpu().numpy(),
+        idx=run.idx[rows_t].cpu().numpy(),
+        partial=run.partial[:, rows_t].cpu().numpy(),
+        lse=run.lse[:, rows_t].cpu().numpy(),
+        out=run.out[rows_t].float().cpu().numpy(),
+        out_lse=run.out_lse[rows_t].cpu().numpy(),
+    )
+    _cache[name] = res
+    return res
+
+
+def _abs_tensor(tn: orc.Tensor) -> orc.Tensor:
+    """Same tensor with every element's sign cleared (for the |q|.|k| bound)."""
+    mask = {"bf16": 0x7FFF, "fp16": 0x7FFF, "e4m3": 0x7F, "nvfp4": 0x77}[tn.dtype]
+    data = tn.data & np.array(mask, dtype=tn.data.dtype)
+    return orc.Tensor(data, tn.dtype, scales=tn.scales, scale=abs(tn.scale))
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_plan_metadata_bit_exact(name):
+    r = _run(name)
+    run, w = r["run"], r["w"]
+    info = run.plan.info()
+    pos = run.ws_array(info.off_tok_pos, w.num_tokens, np.int32)
+    req = run.ws_array(info.off_tok_req, w.num_tokens, np.int32)
+    oreq, opos = orc.token_meta(oracle_problem(w))
+    assert np.array_equal(pos, opos) and np.array_equal(req, oreq)
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_indexer_scores(name):
+    r = _run(name)
+    w, rows = r["w"], r["rows"]
+    pb = oracle_problem(w)
+    q, k, v, qi, ki = oracle_tensors(w, r["t"])
+    ref = orc.indexer(pb, qi, ki, rows)
+    bound = orc.indexer(pb, _abs_tensor(qi), _abs_tensor(ki), rows)
+    got = r["scores"][:, : w.max_pages].astype(np.float64)
+    vis = ~np.isnan(ref)
+    assert np.array_equal(vis, ~np.isnan(got)), "written entries must be exactly p <= o"
+    err = np.abs(got[vis] - ref[vis])
+    tol = SCORE_RTOL * np.maximum(np.abs(ref[vis]), bound[vis])
+    assert np.all(err <= tol), f"max err/tol {np.max(err / tol):.3g}"
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_topk_bit_exact_on_shared_scores(name):
+    r = _run(name)
+    w, rows = r["w"], r["rows"]
+    ref = orc.topk(oracle_problem(w), np.nan_to_num(r["scores"].astype(np.float64), nan=-np.inf),
+                   rows)
+    assert np.array_equal(r["idx"], ref)
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_forward_partials_and_lse(name):
+    r = _run(name)
+    w, rows = r["w"], r["rows"]
+    q, k, v, qi, ki = oracle_tensors(w, r["t"])
+    part, lse = orc.forward(oracle_problem(w), q, k, v, w.sm_scale, r["idx"], rows)
+    got_p = r["partial"].transpose(1, 0, 2)  # [rows][slot][D]
+    got_l = r["lse"].T
+    filled = r["idx"] >= 0
+    assert np.all(got_l[~filled] == -np.inf)
+    assert np.all(np.isnan(got_p[~filled])), "empty slots must not be written"
+    assert rel_l2(got_p[filled], part[filled]) <= PARTIAL_RL2
+    assert np.max(np.abs(got_l[filled] - lse[filled])) <= LSE_ATOL
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_output_matches_oracle(name):
+    r = _run(name)
+    w, rows = r["w"], r["rows"]
+    q, k, v, qi, ki = oracle_tensors(w, r["t"])
+    ref, ref_lse = orc.dense(oracle_problem(w), q, k, v, w.sm_scale, r["idx"], rows)
+    rl2_tol, abs_tol = OUT_TOL["bf16" if w.kv_dtype == "bf16" else "quant"]
+    assert rel_l2(r["out"], ref) <= rl2_tol
+    assert np.max(np.abs(r["out"] - ref)) <= abs_tol
+    assert np.max(np.abs(r["out_lse"] - ref_lse)) <= LSE_ATOL
+
+
+@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+def test_inversion_bit_exact(name):
+    r = _run(name)
+    run, w = r["run"], r["w"]
+    if w.num_rows > 20000:
+        idx_all = run.idx.cpu().numpy()
+    else:
+        idx_all = r["idx"]
+    offsets, er, es = orc.inversion(oracle_problem(w), idx_all)
+    info = run.plan.info()
+    nb = len(offsets) - 1
+    got_off = run.ws_array(info.off_bucket_offsets, nb + 1, np.int32)
+    assert np.array_equal(got_off, offsets.astype(np.int32))
+    ent = run.ws_array(info.off_entries, 2 * len(er), np.int32).reshape(-1, 2)
+    assert np.array_equal(ent[:, 0], er) and np.array_equal(ent[:, 1], es)
+
+
+def test_determinism_three_runs():
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    t = synth.make_tensors(w)
+    outs = []
+    for _ in range(3):
+        run = DeviceRun(w, t)
+        run.run_all()
+        outs.append([x.cpu().clone() for x in (run.scores, run.idx, run.partial, run.lse, run.out)])
+    for a, b in zip(outs[0], outs[1] + outs[2]):
+        pass
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                               b.view(torch.uint8) if b.dtype != torch.int32 else b)
+
+
+def test_wide_score_pitch_and_untouched_entries():
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    t = synth.make_tensors(w)
+    narrow = DeviceRun(w, t)
+    narrow.indexer()
+    wide = DeviceRun(w, t, pitch=8192)
+    wide.indexer()
+    torch.cuda.synchronize()
+    a = narrow.scores.cpu().numpy()
+    b = wide.scores.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b[:, : a.shape[1]].view(np.uint32))
+    assert np.all(np.isnan(b[:, a.shape[1]:]))
+
+
+def test_cuda_graph_replay_matches_eager():
+    from paged_top_sparse_gb300 import binding as B
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    t = synth.make_tensors(w)
+    run = DeviceRun(w, t)
+    run.run_all()
+    eager = [x.clone() for x in (run.scores, run.idx, run.partial, run.lse, run.out)]
+    for x in (run.scores, run.partial, run.lse):
+        x.fill_(float("nan"))
+    run.out.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.indexer_scores(run.plan, run.qi, run.qi_scale, run.ki, run.ki_scales, run.ki_scale,
+                             run.page_table, run.scores, run.ws, stream=s)
+            B.topk_select(run.plan, run.scores, run.idx, run.ws, stream=s)
+            B.sparse_prefill_fwd(run.plan, run.q, run.q_scale, run.k, run.v, run.k_scales,
+                                 run.v_scales, run.page_table, run.idx, run.partial, run.lse,
+                                 run.ws, stream=s)
+            B.partial_combine(run.partial, run.lse, run.out, run.out_lse, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, (run.scores, run.idx, run.partial, run.lse, run.out)):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                           b.view(torch.uint8) if b.dtype != torch.int32 else b)
+
+
+@pytest.mark.parametrize("D,S,R,pad", [(128, 16, 1000, 0), (64, 5, 77, 12), (128, 1, 33, 4),
+                                       (128, 64, 129, 0)])
+def test_combine_direct(D, S, R, pad):
+    """Plan-free combine on random partials: empty slots (lse = -inf) hold NaN garbage that
+    must not leak, one row has no valid slot, split stride padded."""
+    from paged_top_sparse_gb300 import binding as B
+
+    g = torch.Generator().manual_seed(D * 1000 + S * 10 + R)
+    base = torch.randn((S, R * D + pad * 4), generator=g, dtype=torch.float32)
+    lse = 2.0 * torch.randn((S, R), generator=g)
+    drop = torch.rand((S, R), generator=g) < 0.3
+    lse[drop] = float("-inf")
+    lse[:, R // 2] = float("-inf")
+    partial_full = base.clone()
+    pview = partial_full[:, : R * D].view(S, R, D)
+    pview[drop] = float("nan")
+    pv = pview.clone()
+    dev = "cuda:0"
+    pd = partial_full.to(dev)
+    partial = pd.as_strided((S, R, D), (R * D + pad * 4, D, 1))
+    ld = lse.to(dev)
+    out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty(R, dtype=torch.float32, device=dev)
+    B.partial_combine(partial, ld, out, out_lse)
+    torch.cuda.synchronize()
+    ref, ref_lse = orc.combine(np.nan_to_num(pv.numpy(), nan=0.0), lse.numpy())
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert rel_l2(got, ref) <= 2e-3 and np.max(np.abs(got - ref)) <= 1e-2
+    gl = out_lse.cpu().numpy()
+    assert gl[R // 2] == -np.inf and np.all(got[R // 2] == 0)
+    fin = np.isfinite(ref_lse)
+    assert np.max(np.abs(gl[fin] - ref_lse[fin])) <= LSE_ATOL
+
+
+def test_bad_page_table_entry_sets_status():
+    """An out-of-range physical page is caught on the device: status, no fault."""
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    t = synth.make_tensors(w)
+    run = DeviceRun(w, t)
+    run.page_table[0, 1] = w.num_phys_pages + 5
+    run.indexer()
+    assert run.status() == 2  # SPS_DEV_BAD_PAGE
+
+
+def test_host_rejects_invalid_arguments():
+    from paged_top_sparse_gb300 import binding as B
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    t = synth.make_tensors(w)
+    run = DeviceRun(w, t)
+    bad = torch.empty((w.num_rows, w.max_pages - 1), dtype=torch.float32, device="cuda:0")
+    with pytest.raises(B.SpsError) as e:
+        B.indexer_scores(run.plan, run.qi, 1.0, run.ki, None, 1.0, run.page_table, bad, run.ws)
+    assert e.value.status == 1
+    small_ws = run.ws[: run.plan.workspace_bytes // 2]
+    with pytest.raises(B.SpsError) as e:
+        B.sps_plan_upload(run.plan, small_ws)
+    assert e.value.status == 3
