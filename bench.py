@@ -122,6 +122,16 @@ def _algorithmic(w, idx_np):
     }
 
 
+def _workload(args):
+    from paged_top_sparse_gb300 import synth
+
+    if args.tokens == 8192:
+        return synth.workload(WORKLOAD, seed=args.seed)
+    # same shape with another prefill length (used for profiling captures)
+    return synth.workload("custom", seed=args.seed, q_lens=[args.tokens], ctx_lens=[0],
+                          num_q_heads=32, num_kv_heads=2, head_dim=128, top_k=16)
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -131,7 +141,7 @@ def run_gpu(args, rank, world):
     build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w = synth.workload(WORKLOAD, seed=args.seed)
+    w = _workload(args)
     t = synth.make_tensors(w)
     R, K, D = w.num_rows, w.top_k, w.head_dim
 
@@ -272,8 +282,8 @@ def run_gpu(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) BF16 Q/K/V, permuted page table)",
-        "config": {"workload": "prefill 8192 tokens, 32 q / 2 kv heads, head_dim 128, page 128, "
-                               "top-16, BF16 (permuted physical pages)",
+        "config": {"workload": f"prefill {w.num_tokens} tokens, 32 q / 2 kv heads, head_dim 128, "
+                               "page 128, top-16, BF16 (permuted physical pages)",
                    "batch": 1, "seq_len": w.num_tokens, "rows": R,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (256 MB write); per-step CUDA events"},
@@ -288,7 +298,7 @@ def run_gpu(args, rank, world):
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": 9 * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
     }
@@ -354,6 +364,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="prefill length (8192 = the benchmark workload; others for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -119,7 +119,8 @@ typedef struct {
   int64_t off_tok_pos;       /* int32 [T]: absolute position of each token */
   int64_t off_tok_req;       /* int32 [T]: request of each token */
   int64_t off_bucket_offsets;/* int32 [num_buckets + 1]: CSR offsets of the inversion */
-  int64_t off_entries;       /* int32 pairs [max_entries]: (row, slot), rows ascending per bucket */
+  int64_t off_entries;       /* int32 pairs [max_entries]: (row, t*64 + slot), rows ascending per
+                                bucket, t = absolute position of the row's token */
   int64_t off_fwd_task_count;/* int32: number of forward work items built on the device */
 } sps_plan_info;
 
@@ -144,8 +145,9 @@ sps_status sps_plan_get_info(const sps_plan* plan, sps_plan_info* info);
 /*
  * sps_plan_upload -- copies the plan's metadata into `workspace` (device, >= workspace_bytes,
  * 256-byte aligned) on `stream` and clears the device status word.  Call once per (plan,
- * workspace) before the other plan calls, on the same stream.  The plan must stay alive
- * until the copy has completed (the copy reads the plan's pinned host buffer).
+ * workspace) before the other plan calls, on the same stream, and outside CUDA graph capture
+ * (the source is pageable host memory: the call returns once the bytes are staged, so the
+ * plan may be destroyed afterwards).
  */
 sps_status sps_plan_upload(const sps_plan* plan, void* workspace, size_t workspace_bytes,
                            sps_stream_t stream);

@@ -65,11 +65,12 @@ def header_functions() -> list[str]:
 
 
 def lib(path: str | None = None):
-    """Load libsps.so (built in-tree by ``build.build()``); raises if it is absent."""
+    """Load libsps.so (built in-tree by ``build.build()``, or the file named by $SPS_LIB);
+    raises if it is absent."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or _build.LIB
+    path = path or os.environ.get("SPS_LIB") or _build.LIB
     if not os.path.exists(path):
         raise RuntimeError(f"libsps.so not built ({path}); run paged_top_sparse_gb300.build.build()")
     L = ctypes.CDLL(path)

@@ -5,20 +5,27 @@
 // Only the row's own page is causally masked; K/V come through the page table.
 //
 // Design (GB300, one CTA per SM, persistent over the device-built work list):
-//   warp 0     TMA producer: the K and V tiles of the item's physical page (128-byte swizzle),
-//              then per group the 128 query rows, gathered four at a time (tile::gather4)
-//              into a 2-stage Q ring;
+//   (warps 0-3 form the producer/MMA warpgroup, 4-7 the softmax, 8-11 the epilogue;
+//   setmaxnreg moves registers to the softmax)
+//   warp 0     the K and V tiles of the item's physical page by TMA (128-byte swizzle);
+//   warp 2     per group the 128 query rows by TMA tile::gather4 into the same swizzled
+//              layout, in a 2-stage Q ring.  Every global access of the kernel's main loop
+//              runs on the TMA engine: gathering Q through the load/store unit instead left
+//              it queued behind the HBM-bound partial stores.
 //   warp 1     MMA issuer (one thread): S = Q K^T (shared x shared, N = 128 keys) into a
 //              double-buffered TMEM accumulator, and O = P V with P read from TMEM (the
-//              softmax overwrites S with P in place) and V as an MN-major FP16 operand;
-//              S of group g+1 is issued before P.V of group g so softmax and MMA overlap;
-//   warps 2-5  softmax, a thread per row: converts the V tile BF16 -> FP16 in place once per
-//              item; per group, the row max (tcgen05.ld.red.max unless some lane of the warp
-//              owns the page, then the masked element-wise path), p = 2^(s c - m c) rounded
-//              to FP16 into TMEM, l = sum p, LSE = m * scale + ln l straight to global;
-//   warps 6-9  epilogue, a thread per row: O / l from TMEM in 64-column halves into a padded
-//              staging buffer, then one 256-byte bulk store per row and half into
-//              partial[slot][row] (double-buffered staging, stores drain asynchronously).
+//              softmax overwrites S with P in place) and V as an MN-major FP16 operand; it
+//              polls both streams and issues whichever is ready, so S of group g+1 overlaps
+//              the softmax of group g without a late Q tile delaying P.V of group g;
+//   warps 4-7  softmax, a thread per row: converts the V tile BF16 -> FP16 in place once per
+//              item; per group, one TMEM read of the row (tcgen05.ld.red.max gives the max
+//              unless some lane of the warp owns the page, then the masked element-wise
+//              path), p = 2^(s c - m c) rounded to FP16 back into TMEM over S, l = sum p,
+//              LSE = m * scale + ln l straight to global;
+//   warps 8-11 epilogue, a thread per row: O / l from TMEM into a padded staging row, then
+//              one bulk copy of the whole row into partial[slot][row].  The partial stores are
+//              bound by HBM; keeping them on the TMA engine leaves the load/store unit to the
+//              Q gather, which would otherwise queue behind them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -29,8 +36,10 @@ namespace sps {
 namespace {
 
 constexpr int kQS = 2;          // Q ring stages
-constexpr int kThreads = 320;   // 10 warps
-constexpr int kStagePitch = 68; // floats per staging row (64 + 4 pad: conflict-free writes)
+
+constexpr int kThreads = 384;   // 3 warpgroups
+template <int D>
+constexpr int stage_pitch() { return D + 4; }  // floats per staging row (pad: conflict-free)
 
 template <int D>
 struct FwdSmem {
@@ -38,7 +47,7 @@ struct FwdSmem {
   uint8_t k[TILE];
   uint8_t v[TILE];
   uint8_t q[kQS][TILE];
-  float stage[2][128 * kStagePitch];
+  float stage[128 * stage_pitch<D>()];  // one O row per epilogue thread
   float inv_l[2][128];
   int2 rs[2][128];
   uint64_t kv_full, kv_empty, v_ready;
@@ -51,8 +60,9 @@ struct FwdSmem {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, DevPlan p,
+forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap tmQ,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               DevPlan p,
                const int32_t* __restrict__ page_table, float* __restrict__ partial,
                int64_t split_stride, float* __restrict__ lse, int64_t lse_split_stride,
                float q_scale) {
@@ -101,126 +111,171 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const uint32_t tmem = sm.tmem_base;  // S[b] at column 128 b, O[b] at 256 + 128 b
   volatile int* abort_flag = &sm.abort_flag;
 
+  // Registers: the block launches with 168 per thread (384 x 168 = 64512); the producer/MMA
+  // warpgroup gives part of its share to the softmax warpgroup, which holds a whole S row
+  // ((96 + 232 + 168) x 128 = 63488).  Each role's code sits under its own setmaxnreg so the
+  // compiler allocates it within that budget.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer (whole warp)
-    uint32_t kv_it = 0, q_it = 0;
-    for (int ti = blockIdx.x; ti < ntasks; ti += gridDim.x) {
+    // ------------------------------------------------ K/V producer (TMA, one lane)
+    uint32_t kv_it = 0;
+    for (int ti = blockIdx.x; ti < ntasks && lane == 0; ti += gridDim.x) {
       if (*abort_flag) break;
       const FwdTask t = p.fwd_tasks[ti];
       const int gp = t.bucket / p.Hkv, g = t.bucket % p.Hkv;
       const int req = p.page_req[gp];
       const int pg = gp - p.reqs[req].page_base;
-      bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(smem_u32(&sm.kv_empty), (kv_it & 1) ^ 1, abort_flag, status);
-        if (ok) {
-          int phys = __ldg(page_table + (int64_t)req * p.max_pages + pg);
-          if (phys < 0 || phys >= p.num_phys) {
-            set_status(status, DEV_BAD_PAGE);
-            phys = 0;
-          }
-          const uint32_t f = smem_u32(&sm.kv_full);
-          mbar_expect_tx(f, 2 * TILE);
-          const int krow = (phys * p.Hkv + g) * 128;
-          for (int db = 0; db < DB; ++db) {
-            tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * 64, krow, f);
-            tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, f);
-          }
-        }
+      if (!mbar_wait(smem_u32(&sm.kv_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
+      int phys = __ldg(page_table + (int64_t)req * p.max_pages + pg);
+      if (phys < 0 || phys >= p.num_phys) {
+        set_status(status, DEV_BAD_PAGE);
+        phys = 0;
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint32_t f = smem_u32(&sm.kv_full);
+      mbar_expect_tx(f, 2 * TILE);
+      const int krow = (phys * p.Hkv + g) * 128;
+      for (int db = 0; db < DB; ++db) {
+        tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * 64, krow, f);
+        tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, f);
+      }
       ++kv_it;
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------ Q gather (TMA tile::gather4)
+    // Lane l gathers group rows 4l .. 4l+3 (rows past the end of the group repeat its first
+    // row) into the 128-byte-swizzled K-major tile, one gather4 per 64-column block; the
+    // indices of group g+1 are fetched while g is issued.
+    const uint64_t pol_q = l2_policy_evict_last();  // Q rows are re-read once per page
+    uint32_t q_it = 0;
+    bool ok = true;
+    for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
+      const FwdTask t = p.fwd_tasks[ti];
       const int ngroups = (t.count + 127) / 128;
-      for (int grp = 0; grp < ngroups; ++grp) {
-        const int qs = q_it % kQS;
-        if (lane == 0) {
-          ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
-          if (ok) mbar_expect_tx(smem_u32(&sm.q_full[qs]), TILE);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        // lane l gathers group rows 4l .. 4l+3; rows past the end repeat the first row
+      auto fetch_rows = [&](int grp, int (&rows)[4]) {
         const int base = t.entry_begin + grp * 128;
         const int n_in = min(128, t.count - grp * 128);
-        int rows[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = 4 * lane + j;
-          int r = p.entries[base + (i < n_in ? i : 0)].x;
-          if (r < 0 || r >= R) {
-            set_status(status, DEV_OVERFLOW);
-            r = 0;
-          }
-          rows[j] = r;
+          rows[j] = __ldg(&p.entries[base + (i < n_in ? i : 0)].x);
         }
+      };
+      int nxt[4];
+      fetch_rows(0, nxt);
+      for (int grp = 0; grp < ngroups; ++grp) {
+        int rows[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          rows[j] = nxt[j];
+          if (rows[j] < 0 || rows[j] >= R) {
+            set_status(status, DEV_OVERFLOW);
+            rows[j] = 0;
+          }
+        }
+        if (grp + 1 < ngroups) fetch_rows(grp + 1, nxt);
+        const int qs = q_it % kQS;
         const uint32_t qf = smem_u32(&sm.q_full[qs]);
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
+          if (ok) mbar_expect_tx(qf, TILE);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         for (int db = 0; db < DB; ++db)
-          tma_gather4(smem_u32(sm.q[qs]) + db * 16384 + lane * 512, &tmQ, db * 64, rows[0],
-                      rows[1], rows[2], rows[3], qf);
+          tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + lane * 512, &tmQ, db * 64, rows[0],
+                           rows[1], rows[2], rows[3], qf, pol_q);
         ++q_it;
       }
-      if (!ok) break;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer (one thread)
+    // Two streams: S(g) = Q K^T into S[g & 1] once Q(g) has landed, and P.V(g) into O[g & 1]
+    // once the softmax has written P(g).  The thread polls both and issues whichever is ready
+    // (P.V first), so a late Q tile never holds back the P.V and epilogue of earlier groups.
     if (lane == 0) {
-      uint32_t kv_it = 0, q_it = 0, g_issue = 0, g_pv = 0;
-      bool ok = true;
-      // S = Q K^T for global group index gi into S[gi & 1]
-      auto issue_s = [&](uint32_t gi) -> bool {
-        const int qs = q_it % kQS;
-        const int b = gi & 1;
-        if (!mbar_wait(smem_u32(&sm.q_full[qs]), (q_it / kQS) & 1, abort_flag, status)) return false;
-        if (!mbar_wait(smem_u32(&sm.s_free[b]), ((gi >> 1) & 1) ^ 1, abort_flag, status)) return false;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(sm.q[qs]), kb = smem_u32(sm.k);
+      // S cursor (task ti_s, group grp_s) and P.V cursor (ti_p, grp_p); gs / gp count groups
+      int ti_s = blockIdx.x, grp_s = 0, ti_p = blockIdx.x, grp_p = 0;
+      int ng_s = ti_s < ntasks ? (p.fwd_tasks[ti_s].count + 127) / 128 : 0;
+      int ng_p = ng_s;
+      uint32_t gs = 0, gp = 0, q_it = 0, kv_s = 0, kv_p = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (ti_p < ntasks) {
+        bool progressed = false;
+        if (gp < gs) {  // P.V(gp)
+          const int b = gp & 1;
+          const uint32_t ph = (gp >> 1) & 1;
+          if (mbar_try_wait(smem_u32(&sm.p_full[b]), ph) &&
+              mbar_try_wait(smem_u32(&sm.o_empty[b]), ph ^ 1) &&
+              (grp_p != 0 || mbar_try_wait(smem_u32(&sm.v_ready), kv_p & 1))) {
+            tc_fence_after();
+            const uint32_t vb = smem_u32(sm.v);
 #pragma unroll
-        for (int kk = 0; kk < QK_STEPS; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_f16_ss(tmem + b * 128, sdesc_sw128(qb + off, 16, 1024),
-                     sdesc_sw128(kb + off, 16, 1024), IDESC_QK, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)  // 128 keys, K = 16 per step
+              mma_f16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
+                         sdesc_sw128(vb + kk * 2048, 16384, 1024), IDESC_PV, kk > 0);
+            mma_commit(smem_u32(&sm.s_free[b]));
+            mma_commit(smem_u32(&sm.o_full[b]));
+            ++gp;
+            if (++grp_p == ng_p) {  // the item's last P.V: its K/V tiles may be replaced
+              mma_commit(smem_u32(&sm.kv_empty));
+              ++kv_p;
+              grp_p = 0;
+              ti_p += gridDim.x;
+              ng_p = ti_p < ntasks ? (p.fwd_tasks[ti_p].count + 127) / 128 : 0;
+            }
+            progressed = true;
+          }
         }
-        mma_commit(smem_u32(&sm.s_full[b]));
-        mma_commit(smem_u32(&sm.q_empty[qs]));
-        ++q_it;
-        return true;
-      };
-      for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
-        const FwdTask t = p.fwd_tasks[ti];
-        const int ngroups = (t.count + 127) / 128;
-        if (!mbar_wait(smem_u32(&sm.kv_full), kv_it & 1, abort_flag, status)) break;
-        ok = issue_s(g_issue++);
-        for (int grp = 0; grp < ngroups && ok; ++grp) {
-          if (grp + 1 < ngroups) ok = issue_s(g_issue++);
-          if (!ok) break;
-          const int b = g_pv & 1;
-          const uint32_t ph = (g_pv >> 1) & 1;
-          if (!mbar_wait(smem_u32(&sm.p_full[b]), ph, abort_flag, status) ||
-              (grp == 0 && !mbar_wait(smem_u32(&sm.v_ready), kv_it & 1, abort_flag, status)) ||
-              !mbar_wait(smem_u32(&sm.o_empty[b]), ph ^ 1, abort_flag, status)) {
-            ok = false;
+        if (ti_s < ntasks && gs < gp + 2) {  // S(gs)
+          const int qs = q_it % kQS;
+          const int b = gs & 1;
+          if ((grp_s != 0 || mbar_try_wait(smem_u32(&sm.kv_full), kv_s & 1)) &&
+              mbar_try_wait(smem_u32(&sm.q_full[qs]), (q_it / kQS) & 1) &&
+              mbar_try_wait(smem_u32(&sm.s_free[b]), ((gs >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t qb = smem_u32(sm.q[qs]), kb = smem_u32(sm.k);
+#pragma unroll
+            for (int kk = 0; kk < QK_STEPS; ++kk) {
+              const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+              mma_f16_ss(tmem + b * 128, sdesc_sw128(qb + off, 16, 1024),
+                         sdesc_sw128(kb + off, 16, 1024), IDESC_QK, kk > 0);
+            }
+            mma_commit(smem_u32(&sm.s_full[b]));
+            mma_commit(smem_u32(&sm.q_empty[qs]));
+            ++q_it;
+            ++gs;
+            if (++grp_s == ng_s) {
+              ++kv_s;
+              grp_s = 0;
+              ti_s += gridDim.x;
+              ng_s = ti_s < ntasks ? (p.fwd_tasks[ti_s].count + 127) / 128 : 0;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          spins = 0;
+          t_last = globaltimer_ns();
+        } else if ((++spins & 63u) == 0) {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            set_status(status, DEV_TIMEOUT);
+            *abort_flag = 1;
             break;
           }
-          tc_fence_after();
-          const uint32_t vb = smem_u32(sm.v);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 128 keys, K = 16 per step
-            mma_f16_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
-                       sdesc_sw128(vb + kk * 2048, 16384, 1024), IDESC_PV, kk > 0);
-          mma_commit(smem_u32(&sm.s_free[b]));
-          mma_commit(smem_u32(&sm.o_full[b]));
-          ++g_pv;
         }
-        mma_commit(smem_u32(&sm.kv_empty));
-        ++kv_it;
       }
       mma_commit(smem_u32(&sm.done));
       mbar_wait(smem_u32(&sm.done), 0, nullptr, status);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------ softmax: warps 2..5
+  }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    // ------------------------------------------------ softmax: warps 4..7
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
-    const int sm_tid = (warp - 2) * 32 + lane;
+    const int sm_tid = (warp - 4) * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const float c = p.sm_scale * q_scale * 1.4426950408889634f;  // scale * log2(e)
     uint32_t kv_it = 0, g_it = 0;
@@ -251,18 +306,19 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       ++kv_it;
       const int ngroups = (t.count + 127) / 128;
       bool ok = true;
+      // this thread's entry of group g+1 is loaded while group g is processed
+      int2 nxt = row < t.count ? __ldg(&p.entries[t.entry_begin + row]) : make_int2(-1, 0);
       for (int grp = 0; grp < ngroups; ++grp) {
         const int b = g_it & 1;
         const uint32_t ph = (g_it >> 1) & 1;
-        const int ei = grp * 128 + row;
-        const bool valid = ei < t.count;
-        int2 rs = make_int2(-1, -1);
-        int tpos = 0;
-        if (valid) {
-          rs = p.entries[t.entry_begin + ei];
-          if (rs.x < 0 || rs.x >= R || rs.y < 0 || rs.y >= p.K) rs = make_int2(-1, -1);
-          else tpos = __ldg(p.tok_pos + rs.x / p.H);
+        int2 rs = nxt;
+        {
+          const int ei = (grp + 1) * 128 + row;
+          if (grp + 1 < ngroups) nxt = ei < t.count ? __ldg(&p.entries[t.entry_begin + ei]) : make_int2(-1, 0);
         }
+        int tpos = rs.y >> 6;
+        rs.y &= 63;
+        if (rs.x < 0 || rs.x >= R || rs.y >= p.K) rs = make_int2(-1, -1);
         const bool live = rs.x >= 0;
         const bool own = live && (tpos >> 7) == pg;
         const int nvis = own ? (tpos & 127) + 1 : 128;
@@ -270,46 +326,51 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tc_fence_after();
         const uint32_t sbase = tmem + lane_addr + b * 128;
         const bool masked = __any_sync(0xffffffffu, own);
-        // pass 1: raw row max
-        float m = -INFINITY;
+        // the whole S row in one pass: four loads in flight, one wait
+        uint32_t v[4][32];
+        float red[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) red[cc] = tmem_ld32_max(sbase + cc * 32, v[cc]);
+        tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          if (masked) {
-            tmem_ld32(sbase + cc * 32, v);
-            tmem_ld_wait();
+          reg_fence(v[cc]);
+          reg_fence1(red[cc]);
+        }
+        float m;
+        if (masked) {
+          m = -INFINITY;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (cc * 32 + j < nvis) m = fmaxf(m, __uint_as_float(v[j]));
-          } else {
-            const float red = tmem_ld32_max(sbase + cc * 32, v);
-            tmem_ld_wait();
-            m = fmaxf(m, red);
-          }
+              if (cc * 32 + j < nvis) m = fmaxf(m, __uint_as_float(v[cc][j]));
+        } else {
+          m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
         }
         if (!live) m = 0.f;
         const float mc = m * c;
-        // pass 2: p = 2^(s c - m c) as FP16 pairs over the S columns, l = sum p
-        float l = 0.f;
+        // p = 2^(s c - m c) as FP16 pairs written over the S columns, l = sum p (four
+        // independent partial sums)
+        float lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32], pk[16];
-          tmem_ld32(sbase + cc * 32, v);
-          tmem_ld_wait();
+          uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[j]), c, -mc));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[j + 1]), c, -mc));
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[cc][j]), c, -mc));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[cc][j + 1]), c, -mc));
             if (masked) {
               if (cc * 32 + j >= nvis) p0 = 0.f;
               if (cc * 32 + j + 1 >= nvis) p1 = 0.f;
             }
-            l += p0 + p1;
+            lsum[(j >> 1) & 3] += p0 + p1;
             __half2 h2 = __floats2half2_rn(p0, p1);
             pk[j / 2] = *reinterpret_cast<uint32_t*>(&h2);
           }
           tmem_st16(sbase + cc * 16, pk);
         }
+        const float l = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
         tmem_st_wait();
         // row statistics for the epilogue; LSE straight to global
         if (!mbar_wait(smem_u32(&sm.st_empty[b]), ph ^ 1, abort_flag, status)) { ok = false; break; }
@@ -327,16 +388,22 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (!ok) break;
     }
   } else {
-    // ------------------------------------------------ epilogue: warps 6..9
+    // ------------------------------------------------ epilogue: warps 8..11
+    // A thread per row: O / l from TMEM into its padded staging row, then one bulk copy of
+    // the whole row (D x 4 bytes) into partial[slot][row].  The stores run on the TMA engine,
+    // so the load/store unit stays free for the producer's Q gather.
+    constexpr int SP = stage_pitch<D>();
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    uint32_t g_it = 0, st_it = 0;
+    float* srow = sm.stage + row * SP;
+    const uint64_t pol_out = l2_policy_evict_first();  // partials are read once, by the combine
+    uint32_t g_it = 0;
     bool ok = true;
     for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
       const FwdTask t = p.fwd_tasks[ti];
       const int ngroups = (t.count + 127) / 128;
-      for (int grp = 0; grp < ngroups; ++grp) {
+      for (int grp = 0; grp < ngroups; ++grp, ++g_it) {
         const int b = g_it & 1;
         const uint32_t ph = (g_it >> 1) & 1;
         if (!mbar_wait(smem_u32(&sm.o_full[b]), ph, abort_flag, status) ||
@@ -347,37 +414,36 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tc_fence_after();
         const float inv = sm.inv_l[b][row];
         const int2 rs = sm.rs[b][row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.st_empty[b]));
         const uint32_t obase = tmem + lane_addr + 256 + b * 128;
+        bulk_wait_read<0>();  // this row's previous store has finished reading the staging row
 #pragma unroll
-        for (int hh = 0; hh < DB; ++hh) {
-          const int sb = st_it & 1;
-          bulk_wait_read<1>();  // this thread's store from staging[sb] two halves ago is done
-          float* srow = sm.stage[sb] + row * kStagePitch;
+        for (int hh = 0; hh < D / 64; ++hh) {
+          uint32_t v[2][32];
+          tmem_ld32(obase + hh * 64, v[0]);
+          tmem_ld32(obase + hh * 64 + 32, v[1]);
+          tmem_ld_wait();
+          reg_fence(v[0]);
+          reg_fence(v[1]);
+          if (hh == D / 64 - 1) {  // O[b] fully read: hand the accumulator back to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.o_empty[b]));
+          }
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(obase + hh * 64 + cc * 32, v);
-            tmem_ld_wait();
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(srow + cc * 32 + j) =
-                  make_float4(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv,
-                              __uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
-          }
-          fence_proxy_async_smem();
-          if (rs.x >= 0)
-            bulk_store(partial + (int64_t)rs.y * split_stride + (int64_t)rs.x * D + hh * 64,
-                       smem_u32(srow), 256);
-          bulk_commit();
-          ++st_it;
+              *reinterpret_cast<float4*>(srow + hh * 64 + cc * 32 + j) = make_float4(
+                  __uint_as_float(v[cc][j]) * inv, __uint_as_float(v[cc][j + 1]) * inv,
+                  __uint_as_float(v[cc][j + 2]) * inv, __uint_as_float(v[cc][j + 3]) * inv);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&sm.o_empty[b]));
-          mbar_arrive(smem_u32(&sm.st_empty[b]));
-        }
-        ++g_it;
+        fence_proxy_async_smem();
+        if (rs.x >= 0)
+          bulk_store_hint(partial + (int64_t)rs.y * split_stride + (int64_t)rs.x * D,
+                          smem_u32(srow), D * 4, pol_out);
+        bulk_commit();
       }
     }
     bulk_wait_all<0>();
@@ -405,7 +471,7 @@ cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const v
   auto kern = forward_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, st>>>(tmQ, tmK, tmV, p, page_table, partial, split_stride,
+  kern<<<num_sms(), kThreads, smem, st>>>(q, tmQ, tmK, tmV, p, page_table, partial, split_stride,
                                           lse, lse_split_stride, q_scale);
   return cudaGetLastError();
 }

@@ -50,10 +50,11 @@ struct sps_plan {
   std::vector<int32_t> page_req;  // [total_pages]
   std::vector<IdxTask> idx_tasks;
   int64_t T = 0, R = 0, num_buckets = 0, max_entries = 0, max_fwd_tasks = 0;
-  int64_t total_pages = 0, bm_total_words = 0;
+  int64_t total_pages = 0, bm_total_words = 0, num_chunks = 0;
   // workspace layout (bytes)
   int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
-          off_page_req = 0, off_idx_tasks = 0, off_bitmap = 0, off_bucket_count = 0,
+          off_page_req = 0, off_idx_tasks = 0, off_bitmap = 0, off_chunk_offsets = 0,
+          off_word_pos = 0,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
   int64_t upload_bytes = 0;  // [off_tok_pos, off_tok_pos + upload_bytes) comes from `blob`
   std::vector<uint8_t> blob;
@@ -89,7 +90,7 @@ sps_status validate_problem(const sps_problem* p) {
     if (p->q_lens[b] < 0 || p->ctx_lens[b] < 0)
       return fail(SPS_EINVAL, "request %d: negative q_len/ctx_len", b);
     int64_t last = (int64_t)p->ctx_lens[b] + p->q_lens[b] - 1;
-    if (last >= (int64_t)1 << 30) return fail(SPS_EINVAL, "request %d: sequence too long", b);
+    if (last >= (int64_t)1 << 24) return fail(SPS_EINVAL, "request %d: sequence too long", b);
     int64_t np = p->q_lens[b] > 0 ? last / kPage + 1 : 0;
     if (np > p->max_pages_per_req)
       return fail(SPS_EINVAL, "request %d needs %lld pages > max_pages_per_req %d", b,
@@ -183,6 +184,9 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
     ri.page_base = page_base;
     ri.bm_words = (int32_t)((int64_t(ri.q_len) * Hg + 31) / 32);
     ri.bm_base = bm_base;
+    ri.ch_per_bucket = (ri.bm_words + kChunkWords - 1) / kChunkWords;
+    ri.ch_base = (int32_t)pl->num_chunks;
+    pl->num_chunks += (int64_t)ri.npages * p.num_kv_heads * ri.ch_per_bucket;
     for (int i = 0; i < ri.q_len; ++i) {
       tok_pos.push_back(ri.ctx + i);
       tok_req.push_back(b);
@@ -219,7 +223,8 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->off_idx_tasks = take(sizeof(IdxTask) * std::max<size_t>(1, pl->idx_tasks.size()));
   int64_t upload_end = off;
   pl->off_bitmap = take(4 * std::max<int64_t>(1, pl->bm_total_words));
-  pl->off_bucket_count = take(4 * std::max<int64_t>(1, pl->num_buckets));
+  pl->off_chunk_offsets = take(4 * (pl->num_chunks + 1));
+  pl->off_word_pos = take(4 * std::max<int64_t>(1, pl->bm_total_words));
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
@@ -296,7 +301,9 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.page_req = reinterpret_cast<const int32_t*>(base + pl->off_page_req);
   d.idx_tasks = reinterpret_cast<const IdxTask*>(base + pl->off_idx_tasks);
   d.bitmap = reinterpret_cast<uint32_t*>(base + pl->off_bitmap);
-  d.bucket_count = reinterpret_cast<int32_t*>(base + pl->off_bucket_count);
+  d.num_chunks = (int32_t)pl->num_chunks;
+  d.chunk_offsets = reinterpret_cast<int32_t*>(base + pl->off_chunk_offsets);
+  d.word_pos = reinterpret_cast<int32_t*>(base + pl->off_word_pos);
   d.bucket_offsets = reinterpret_cast<int32_t*>(base + pl->off_bucket_offsets);
   d.entries = reinterpret_cast<int2*>(base + pl->off_entries);
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);

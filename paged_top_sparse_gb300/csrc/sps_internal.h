@@ -3,13 +3,14 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/sparse_prefill.h"
+#include "sparse_prefill.h"
 
 namespace sps {
 
 constexpr int kPage = 128;         // tokens per KV page
 constexpr int kMaxTopK = 64;
 constexpr int kFwdTaskGroups = 8;  // 128-row query groups per forward work item
+constexpr int kChunkWords = 2048;  // bitmap words per prefix-scan chunk (256 threads x 8)
 
 // One request of the batch, as the kernels see it.
 struct ReqInfo {
@@ -20,7 +21,9 @@ struct ReqInfo {
   int32_t page_base;  // running sum of npages over earlier requests
   int32_t bm_base;    // first selection-bitmap word of the request
   int32_t bm_words;   // words per (page, KV head) bucket: ceil(q_len * H/H_kv / 32)
-  int32_t pad;
+  int32_t ch_base;    // first bitmap chunk of the request
+  int32_t ch_per_bucket;  // chunks per bucket: ceil(bm_words / kChunkWords)
+  int32_t pad[5];
 };
 
 // Indexer work item: query tile (<=128 tokens of one request, 1-2 query heads of one KV
@@ -50,9 +53,11 @@ struct DevPlan {
   const int32_t* page_req;  // [total_pages]: request of each global page slot
   const IdxTask* idx_tasks; // [n_idx_tasks]
   uint32_t* bitmap;         // [bm_total_words]
-  int32_t* bucket_count;    // [num_buckets]
+  int32_t num_chunks;       // bitmap chunks (buckets x chunks per bucket)
+  int32_t* chunk_offsets;   // [num_chunks + 1]: entries before each chunk
+  int32_t* word_pos;        // [bm_total_words]: entries before each bitmap word
   int32_t* bucket_offsets;  // [num_buckets + 1]
-  int2* entries;            // [max_entries] (row, slot)
+  int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
 };
 

@@ -164,7 +164,10 @@ def test_inversion_bit_exact(name):
     got_off = run.ws_array(info.off_bucket_offsets, nb + 1, np.int32)
     assert np.array_equal(got_off, offsets.astype(np.int32))
     ent = run.ws_array(info.off_entries, 2 * len(er), np.int32).reshape(-1, 2)
-    assert np.array_equal(ent[:, 0], er) and np.array_equal(ent[:, 1], es)
+    _, tok_pos = orc.token_meta(oracle_problem(w))
+    assert np.array_equal(ent[:, 0], er)
+    assert np.array_equal(ent[:, 1] & 63, es)
+    assert np.array_equal(ent[:, 1] >> 6, tok_pos[er // w.num_q_heads])
 
 
 def test_determinism_three_runs():
