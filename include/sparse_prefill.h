@@ -230,6 +230,43 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
                            int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sparse_prefill_fwd_noalloc -- sparse_prefill_fwd for callers that cannot allocate device
+ * memory.  (No counterpart on the pages: this is an interface convenience of this library.)
+ *
+ * Who needs it: code that must not call cudaMalloc or hand out device buffers of its own --
+ * for example a plug-in called from inside another runtime whose memory pool it cannot reach,
+ * a serving loop that forbids new device allocations once it is warm, or a C caller with a
+ * fixed device-memory budget.  Such a caller can still pass its inputs and outputs, but it has
+ * no workspace to give; this variant keeps the forward's scratch (the plan's metadata and the
+ * page -> row inversion) in a fixed array inside the library instead.
+ *
+ * Arguments are those of sparse_prefill_fwd without the workspace, plus
+ *   dev_status  device int32 or NULL: where the kernels record device-side errors
+ *               (SPS_DEV_*; the caller clears it).  With NULL such errors go unreported.
+ * The plan needs no sps_plan_upload: this call copies the plan's metadata into the array.
+ *
+ * Rules.
+ *   - The array holds 48 MiB per device and every GPU that loads the library keeps it until
+ *     the process exits.  A plan whose workspace_bytes exceeds 48 MiB is rejected with
+ *     SPS_ENOSPACE (for example 16K tokens x 32 heads x top-16 needs more); split the batch or
+ *     use sparse_prefill_fwd.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture on the device.
+ *   - All calls on a device share the one array, and it keeps the last call's contents (each
+ *     call clears and rewrites what it needs).  Calls whose work overlaps on the GPU -- on
+ *     different streams, or from different host threads -- race and corrupt each other; order
+ *     them on one stream.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+sps_status sparse_prefill_fwd_noalloc(const sps_plan* plan, const void* q, float q_scale,
+                                      const void* k_cache, const void* v_cache,
+                                      const void* k_scales, const void* v_scales,
+                                      const int32_t* page_table, const int32_t* idx,
+                                      float* partial, int64_t split_stride, float* lse,
+                                      int64_t lse_split_stride, int32_t* dev_status,
+                                      sps_stream_t stream);
+
+/*
  * sps_read_device_status -- synchronous: waits for the device, then copies the plan
  * workspace's status word into *code (SPS_DEV_*).  Returns SPS_EDEVICE when it is non-zero.
  */

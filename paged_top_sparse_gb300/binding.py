@@ -85,10 +85,13 @@ def lib(path: str | None = None):
     L.topk_select.argtypes = [vp, vp, i64, vp, vp, vp]
     L.sparse_prefill_fwd.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
     L.partial_combine.argtypes = [i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, vp, vp]
+    L.sparse_prefill_fwd_noalloc.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64,
+                                             vp, vp]
     L.sps_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     L.sps_last_error.restype = ctypes.c_char_p
     for name in ("sparse_prefill_plan", "sps_plan_get_info", "sps_plan_upload", "indexer_scores",
-                 "topk_select", "sparse_prefill_fwd", "partial_combine", "sps_read_device_status"):
+                 "topk_select", "sparse_prefill_fwd", "partial_combine", "sps_read_device_status",
+                 "sparse_prefill_fwd_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -174,6 +177,16 @@ def sparse_prefill_fwd(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_sca
                                     _ptr(v_cache), _ptr(k_scales), _ptr(v_scales), _ptr(page_table),
                                     _ptr(idx), _ptr(partial), partial.stride(0), _ptr(lse),
                                     lse.stride(0), _ptr(workspace), _stream(stream)))
+
+
+def sparse_prefill_fwd_noalloc(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
+                               page_table, idx, partial, lse, dev_status=None, stream=None):
+    """sparse_prefill_fwd without a workspace: the library's own fixed scratch array is used
+    (for callers that cannot allocate device memory; see the header for the rules)."""
+    _check(lib().sparse_prefill_fwd_noalloc(
+        plan.handle, _ptr(q), float(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales),
+        _ptr(v_scales), _ptr(page_table), _ptr(idx), _ptr(partial), partial.stride(0), _ptr(lse),
+        lse.stride(0), _ptr(dev_status), _stream(stream)))
 
 
 def partial_combine(partial, lse, out, out_lse=None, dev_status=None, stream=None):

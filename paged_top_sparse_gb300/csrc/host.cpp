@@ -524,3 +524,55 @@ int num_sms() {
 }
 
 }  // namespace sps
+
+// ------------------------------------------------------------------ scratch-array forward
+// Used by sparse_prefill_fwd_noalloc (noalloc.cu), which owns the scratch array: the same
+// checks and launches as sparse_prefill_fwd, with the plan's metadata copied into the given
+// scratch area first (the caller has no workspace to upload into).
+sps_status sps_internal_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+sps_status sps_internal_fwd_noalloc(const sps_plan* pl, const void* q, float q_scale,
+                                    const void* k_cache, const void* v_cache, const void* k_scales,
+                                    const void* v_scales, const int32_t* page_table,
+                                    const int32_t* idx, float* partial, int64_t split_stride,
+                                    float* lse, int64_t lse_split_stride, void* scratch,
+                                    size_t scratch_bytes, int32_t* dev_status,
+                                    sps_stream_t stream) {
+  if (!pl) return fail(SPS_EINVAL, "plan is NULL");
+  const sps_problem& p = pl->pb;
+  if (!q || !k_cache || !v_cache || !page_table || !idx || !partial || !lse)
+    return fail(SPS_EINVAL, "sparse_prefill_fwd_noalloc: NULL input/output pointer");
+  if (p.kv_dtype == SPS_NVFP4 && (!k_scales || !v_scales))
+    return fail(SPS_EINVAL, "sparse_prefill_fwd_noalloc: NVFP4 K/V need k_scales and v_scales");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      (k_scales && !aligned(k_scales, 16)) || (v_scales && !aligned(v_scales, 16)))
+    return fail(SPS_EINVAL, "sparse_prefill_fwd_noalloc: q/k/v buffers must be 16-byte aligned");
+  if (!aligned(partial, 16)) return fail(SPS_EINVAL, "partial must be 16-byte aligned");
+  if (split_stride < pl->R * p.head_dim || split_stride % 4)
+    return fail(SPS_EINVAL, "split_stride must be >= rows*head_dim and a multiple of 4");
+  if (lse_split_stride < pl->R) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
+  if (!std::isfinite(q_scale)) return fail(SPS_EINVAL, "q_scale must be finite");
+  if (dev_status && !aligned(dev_status, 4)) return fail(SPS_EINVAL, "dev_status misaligned");
+  if ((int64_t)scratch_bytes < pl->ws_bytes)
+    return fail(SPS_ENOSPACE,
+                "sparse_prefill_fwd_noalloc: this batch needs %lld bytes of scratch, the built-in "
+                "array holds %zu; split the batch or use sparse_prefill_fwd with a workspace",
+                (long long)pl->ws_bytes, scratch_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  // the array keeps the previous call's contents: zero the status word and counters, then
+  // write this plan's metadata over the old one
+  cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch header)");
+  e = cudaMemcpyAsync(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes,
+                      cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan metadata -> scratch)");
+  DevPlan d = make_dev_plan(pl, scratch);
+  if (dev_status) d.status = dev_status;
+  e = launch_inversion(d, idx, lse, lse_split_stride, s);
+  if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
+  return launched(launch_forward(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
+                                 k_scales, v_scales, page_table, partial, split_stride, lse,
+                                 lse_split_stride, s),
+                  "forward launch");
+}
