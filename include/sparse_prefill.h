@@ -230,6 +230,21 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
                            int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sps_dequantize -- exact conversion of quantised inputs to FP16 (the dequant step of "MSA PR
+ * 21: Q8KV4 paged sparse prefill", Build the prefill for SM107: an E2M1 code times its E4M3
+ * scale is exact in FP16).  The indexer and the forward run it internally on quantised plans.
+ *   in_dtype  SPS_E4M3: `in` holds n one-byte codes (16-byte aligned);
+ *             SPS_NVFP4: `in` holds n/2 bytes of packed E2M1 codes, the even element in the
+ *             low nibble (8-byte aligned), and `scales` n/16 E4M3 scales, one per 16
+ *             consecutive elements
+ *   n         number of elements, a multiple of 16
+ *   out_f16   device FP16 [n] (16-byte aligned): code (E4M3), or code x scale (NVFP4), with no
+ *             per-tensor scale applied.  Every result is exact (NaN codes give NaN).
+ */
+sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales, int64_t n,
+                          void* out_f16, sps_stream_t stream);
+
+/*
  * sparse_prefill_fwd_noalloc -- sparse_prefill_fwd for callers that cannot allocate device
  * memory.  (No counterpart on the pages: this is an interface convenience of this library.)
  *

@@ -88,10 +88,11 @@ def lib(path: str | None = None):
     L.sparse_prefill_fwd_noalloc.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64,
                                              vp, vp]
     L.sps_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    L.sps_dequantize.argtypes = [ctypes.c_int, vp, vp, i64, vp, vp]
     L.sps_last_error.restype = ctypes.c_char_p
     for name in ("sparse_prefill_plan", "sps_plan_get_info", "sps_plan_upload", "indexer_scores",
                  "topk_select", "sparse_prefill_fwd", "partial_combine", "sps_read_device_status",
-                 "sparse_prefill_fwd_noalloc"):
+                 "sparse_prefill_fwd_noalloc", "sps_dequantize"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -195,6 +196,12 @@ def partial_combine(partial, lse, out, out_lse=None, dev_status=None, stream=Non
     _check(lib().partial_combine(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
                                  lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
                                  _ptr(dev_status), _stream(stream)))
+
+
+def sps_dequantize(in_dtype: str, data, scales, n: int, out_f16, stream=None):
+    """Exact E4M3 / NVFP4 -> FP16 of n elements into ``out_f16`` (see the header)."""
+    _check(lib().sps_dequantize(DTYPE_CODES[in_dtype], _ptr(data), _ptr(scales), int(n),
+                                _ptr(out_f16), _stream(stream)))
 
 
 def sps_read_device_status(plan: Plan, workspace) -> int:

@@ -1,0 +1,97 @@
+// dequant.cu -- exact dequantisation of E4M3 and NVFP4 data to FP16 ("MSA PR 21: Q8KV4 paged
+// sparse prefill", Build the prefill for SM107: an E2M1 code times its E4M3 scale is exact in
+// FP16, so the product needs no rounding).
+//
+//   E4M3  -> FP16: every E4M3 value is an FP16 value (3 mantissa bits, exponents 2^-9..2^8).
+//   NVFP4 -> FP16: E2M1 code (hardware cvt to FP16) times the E4M3 scale of its 16-element
+//                  block (cvt to FP16), one FP16 multiply that is exact: the product has at
+//                  most 6 significant bits and lies within [2^-10, 2688].
+//
+// Streaming kernels (grid-stride, 16 elements per thread per step); the indexer and the
+// forward run them on quantised inputs before their FP16 tensor-core paths.
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sps_internal.h"
+
+namespace sps {
+
+// Two E4M3 codes (low byte = first element) -> f16x2 (low half = first element).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+// Two E2M1 codes in one byte (low nibble = first element) -> f16x2.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint16_t byte_in_low) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tmov.b16 {t, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "h"(byte_in_low));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
+  __half2 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&z);
+}
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+e4m3_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int64_t n16) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(in + i);  // 16 codes
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[2 * j] = cvt_e4m3x2((uint16_t)(w[j] & 0xffff));
+      h[2 * j + 1] = cvt_e4m3x2((uint16_t)(w[j] >> 16));
+    }
+    out[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+nvfp4_to_f16_kernel(const uint2* __restrict__ codes, const uint8_t* __restrict__ scales,
+                    uint4* __restrict__ out, int64_t nblocks) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblocks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint2 c = __ldg(codes + i);  // 16 codes of one 16-element block
+    const uint8_t sb = __ldg(scales + i);
+    const uint32_t s2 = cvt_e4m3x2((uint16_t)(sb | (sb << 8)));  // (scale, scale)
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        h[4 * j + b] = hmul2_u32(cvt_e2m1x2((uint16_t)((w[j] >> (8 * b)) & 0xff)), s2);
+    out[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
+                           void* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t units = n / 16;
+  const unsigned grid = (unsigned)std::min<int64_t>((units + 255) / 256, 8LL * num_sms());
+  if (dt == SPS_E4M3)
+    e4m3_to_f16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(in),
+                                              static_cast<uint4*>(out), units);
+  else if (dt == SPS_NVFP4)
+    nvfp4_to_f16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint2*>(in),
+                                               static_cast<const uint8_t*>(scales),
+                                               static_cast<uint4*>(out), units);
+  else
+    return cudaErrorNotSupported;
+  return cudaGetLastError();
+}
+
+}  // namespace sps

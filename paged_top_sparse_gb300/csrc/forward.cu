@@ -58,7 +58,9 @@ struct FwdSmem {
   int abort_flag;
 };
 
-template <int D>
+// F16IN: Q, K and V arrive as FP16 (dequantised inputs) instead of BF16; then S = Q K^T runs
+// on FP16 operands and V needs no conversion.
+template <int D, bool F16IN>
 __global__ void __launch_bounds__(kThreads, 1)
 forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -70,7 +72,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   constexpr int DB = D / 64;          // 128-byte column blocks of a 16-bit row
   constexpr int TILE = Smem::TILE;
   constexpr int QK_STEPS = D / 16;
-  constexpr uint32_t IDESC_QK = idesc_mma(true, true, 128, 128, false, false);
+  constexpr uint32_t IDESC_QK = idesc_mma(!F16IN, !F16IN, 128, 128, false, false);
   constexpr uint32_t IDESC_PV = idesc_mma(false, false, 128, D, false, true);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -285,7 +287,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       const int pg = gp - p.reqs[p.page_req[gp]].page_base;
       // V tile: BF16 -> FP16 in place (same swizzled positions)
       if (!mbar_wait(smem_u32(&sm.kv_full), kv_it & 1, abort_flag, status)) break;
-      {
+      if (!F16IN) {
         uint4* v4 = reinterpret_cast<uint4*>(sm.v);
         for (int i = sm_tid; i < TILE / 16; i += 128) {
           uint4 x = v4[i];
@@ -300,9 +302,9 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
           v4[i] = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready));
       ++kv_it;
       const int ngroups = (t.count + 127) / 128;
       bool ok = true;
@@ -456,19 +458,20 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   }
 }
 
-template <int D>
+template <int D, bool F16IN>
 cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const void* vc,
                         const int32_t* page_table, float* partial, int64_t split_stride,
                         float* lse, int64_t lse_split_stride, float q_scale, cudaStream_t st) {
   alignas(64) CUtensorMap tmQ, tmK, tmV;
   const uint64_t R = (uint64_t)p.T * p.H;
   const uint64_t kv_rows = (uint64_t)p.num_phys * p.Hkv * 128;
-  if (!encode_tmap_2d(&tmQ, 0, const_cast<void*>(q), D, R, (uint64_t)D * 2, 64, 1, true) ||
-      !encode_tmap_2d(&tmK, 0, const_cast<void*>(kc), D, kv_rows, (uint64_t)D * 2, 64, 128, true) ||
-      !encode_tmap_2d(&tmV, 0, const_cast<void*>(vc), D, kv_rows, (uint64_t)D * 2, 64, 128, true))
+  const int dt = F16IN ? 1 : 0;  // tensor-map element type: BF16 or FP16
+  if (!encode_tmap_2d(&tmQ, dt, const_cast<void*>(q), D, R, (uint64_t)D * 2, 64, 1, true) ||
+      !encode_tmap_2d(&tmK, dt, const_cast<void*>(kc), D, kv_rows, (uint64_t)D * 2, 64, 128, true) ||
+      !encode_tmap_2d(&tmV, dt, const_cast<void*>(vc), D, kv_rows, (uint64_t)D * 2, 64, 128, true))
     return cudaErrorInvalidValue;
   const int smem = (int)sizeof(FwdSmem<D>) + 1024;
-  auto kern = forward_kernel<D>;
+  auto kern = forward_kernel<D, F16IN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreads, smem, st>>>(q, tmQ, tmK, tmV, p, page_table, partial, split_stride,
@@ -483,14 +486,27 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
                            const void* vs, const int32_t* page_table, float* partial,
                            int64_t split_stride, float* lse, int64_t lse_split_stride,
                            cudaStream_t st) {
-  (void)ks;
-  (void)vs;
   if (qt == SPS_BF16 && kvt == SPS_BF16) {
     if (p.D == 128)
-      return run_forward<128>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                              lse_split_stride, q_scale, st);
-    return run_forward<64>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                           lse_split_stride, q_scale, st);
+      return run_forward<128, false>(p, q, kc, vc, page_table, partial, split_stride, lse,
+                                     lse_split_stride, q_scale, st);
+    return run_forward<64, false>(p, q, kc, vc, page_table, partial, split_stride, lse,
+                                  lse_split_stride, q_scale, st);
+  }
+  if (qt == SPS_E4M3 && kvt == SPS_NVFP4) {
+    // exact FP16 copies of the E4M3 codes and of the NVFP4 products; q_scale stays in the
+    // softmax exponent
+    if (!p.qconv || !p.kconv || !p.vconv) return cudaErrorInvalidValue;
+    const int64_t ce = (int64_t)p.num_phys * p.Hkv * 128 * p.D;
+    cudaError_t e = launch_dequant(SPS_E4M3, q, nullptr, (int64_t)p.T * p.H * p.D, p.qconv, st);
+    if (e == cudaSuccess) e = launch_dequant(SPS_NVFP4, kc, ks, ce, p.kconv, st);
+    if (e == cudaSuccess) e = launch_dequant(SPS_NVFP4, vc, vs, ce, p.vconv, st);
+    if (e != cudaSuccess) return e;
+    if (p.D == 128)
+      return run_forward<128, true>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
+                                    split_stride, lse, lse_split_stride, q_scale, st);
+    return run_forward<64, true>(p, p.qconv, p.kconv, p.vconv, page_table, partial, split_stride,
+                                 lse, lse_split_stride, q_scale, st);
   }
   return cudaErrorNotSupported;
 }

@@ -54,7 +54,7 @@ struct sps_plan {
   // workspace layout (bytes)
   int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
           off_page_req = 0, off_idx_tasks = 0, off_bitmap = 0, off_chunk_offsets = 0,
-          off_word_pos = 0,
+          off_word_pos = 0, off_qconv = -1, off_kconv = -1, off_vconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
   int64_t upload_bytes = 0;  // [off_tok_pos, off_tok_pos + upload_bytes) comes from `blob`
   std::vector<uint8_t> blob;
@@ -85,6 +85,8 @@ sps_status validate_problem(const sps_problem* p) {
                 (p->idx_q_dtype == SPS_E4M3 && p->idx_k_dtype == SPS_NVFP4);
   if (!idx_ok)
     return fail(SPS_EUNSUPPORTED, "indexer dtypes must be BF16/BF16, E4M3/E4M3 or E4M3/NVFP4");
+  if (p->idx_q_dtype == SPS_E4M3 && p->idx_k_dtype == SPS_E4M3 && p->head_dim != 128)
+    return fail(SPS_EUNSUPPORTED, "the E4M3 x E4M3 indexer needs head_dim 128");
   int64_t T = 0;
   for (int b = 0; b < p->batch; ++b) {
     if (p->q_lens[b] < 0 || p->ctx_lens[b] < 0)
@@ -228,6 +230,14 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
+  // FP16 staging of quantised inputs for the tensor-core paths (E4M3 x E4M3 indexing runs on
+  // the FP8 tensor core directly and needs none)
+  const bool idx_fp16 = p.idx_k_dtype == SPS_NVFP4;
+  const int64_t cache_elems = (int64_t)p.num_phys_pages * p.num_kv_heads * kPage * p.head_dim;
+  if (p.q_dtype == SPS_E4M3 || (idx_fp16 && p.idx_q_dtype == SPS_E4M3))
+    pl->off_qconv = take(2 * pl->R * p.head_dim);
+  if (p.kv_dtype == SPS_NVFP4 || idx_fp16) pl->off_kconv = take(2 * cache_elems);
+  if (p.kv_dtype == SPS_NVFP4) pl->off_vconv = take(2 * cache_elems);
   pl->ws_bytes = off;
 
   // the host image of [off_tok_pos, upload_end)
@@ -307,6 +317,9 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.bucket_offsets = reinterpret_cast<int32_t*>(base + pl->off_bucket_offsets);
   d.entries = reinterpret_cast<int2*>(base + pl->off_entries);
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
+  d.qconv = pl->off_qconv >= 0 ? base + pl->off_qconv : nullptr;
+  d.kconv = pl->off_kconv >= 0 ? base + pl->off_kconv : nullptr;
+  d.vconv = pl->off_vconv >= 0 ? base + pl->off_vconv : nullptr;
   return d;
 }
 
@@ -318,6 +331,9 @@ sps_status check_plan_ws(const sps_plan* pl, const void* ws) {
 }
 
 sps_status launched(cudaError_t e, const char* what) {
+  if (e == cudaErrorNotSupported)
+    return fail(SPS_EUNSUPPORTED, "%s: not implemented for this dtype combination / head_dim",
+                what);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return SPS_OK;
 }
@@ -436,6 +452,22 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
                                  lse_split_stride, out_bf16, out_row_stride, out_lse, dev_status,
                                  reinterpret_cast<cudaStream_t>(stream)),
                   "combine launch");
+}
+
+sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales, int64_t n,
+                          void* out_f16, sps_stream_t stream) {
+  if (in_dtype != SPS_E4M3 && in_dtype != SPS_NVFP4)
+    return fail(SPS_EUNSUPPORTED, "sps_dequantize: input must be E4M3 or NVFP4");
+  if (n < 0 || n % 16) return fail(SPS_EINVAL, "sps_dequantize: n must be a multiple of 16");
+  if (n == 0) return SPS_OK;
+  if (!in || !out_f16 || (in_dtype == SPS_NVFP4 && !scales))
+    return fail(SPS_EINVAL, "sps_dequantize: NULL pointer");
+  if (!aligned(in, in_dtype == SPS_E4M3 ? 16 : 8) || !aligned(out_f16, 16))
+    return fail(SPS_EINVAL, "sps_dequantize: input must be %d-byte and output 16-byte aligned",
+                in_dtype == SPS_E4M3 ? 16 : 8);
+  return launched(launch_dequant(in_dtype, in, scales, n, out_f16,
+                                 reinterpret_cast<cudaStream_t>(stream)),
+                  "dequant launch");
 }
 
 sps_status sps_read_device_status(const sps_plan* pl, const void* ws, int32_t* code) {

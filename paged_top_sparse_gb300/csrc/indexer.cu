@@ -258,7 +258,6 @@ cudaError_t launch_indexer(const DevPlan& p, sps_dtype qt, sps_dtype kt, const v
                            float q_scale, const void* kc, const void* kscales, float k_scale,
                            const int32_t* page_table, float* scores, int64_t pitch,
                            cudaStream_t st) {
-  (void)kscales;
   const float scale = q_scale * k_scale;
   if (qt == SPS_BF16 && kt == SPS_BF16) {
     if (p.D == 128) return run_indexer<256, false, true>(p, 0, q, kc, page_table, scores, pitch, scale, st);
@@ -266,6 +265,19 @@ cudaError_t launch_indexer(const DevPlan& p, sps_dtype qt, sps_dtype kt, const v
   }
   if (qt == SPS_E4M3 && kt == SPS_E4M3 && p.D == 128)
     return run_indexer<128, true, false>(p, 2, q, kc, page_table, scores, pitch, scale, st);
+  if (qt == SPS_E4M3 && kt == SPS_NVFP4) {
+    // E4M3 codes and NVFP4 products are exact in FP16: convert both, then the FP16 MMA path
+    // (the per-tensor scales stay in the FP32 epilogue)
+    if (!p.qconv || !p.kconv) return cudaErrorInvalidValue;
+    cudaError_t e = launch_dequant(SPS_E4M3, q, nullptr, (int64_t)p.T * p.H * p.D, p.qconv, st);
+    if (e != cudaSuccess) return e;
+    e = launch_dequant(SPS_NVFP4, kc, kscales, (int64_t)p.num_phys * p.Hkv * 128 * p.D, p.kconv,
+                       st);
+    if (e != cudaSuccess) return e;
+    if (p.D == 128)
+      return run_indexer<256, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch, scale, st);
+    return run_indexer<128, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch, scale, st);
+  }
   return cudaErrorNotSupported;
 }
 

@@ -59,6 +59,11 @@ struct DevPlan {
   int32_t* bucket_offsets;  // [num_buckets + 1]
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
+  // FP16 copies of quantised inputs (null when the plan has none): Q [T][H][D] and K, V
+  // caches [num_phys][H_kv][128][D]; each call that needs one converts into it first
+  void* qconv;
+  void* kconv;
+  void* vconv;
 };
 
 // Launchers (one per kernel file).  Return cudaSuccess or the launch error.
@@ -79,6 +84,10 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
                            const void* vs, const int32_t* page_table, float* partial,
                            int64_t split_stride, float* lse, int64_t lse_split_stride,
                            cudaStream_t st);
+
+// Exact E4M3 / NVFP4 -> FP16 conversion of n elements (n % 16 == 0).
+cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
+                           void* out, cudaStream_t st);
 
 // Tensor-map encoding through the driver entry point (no link against libcuda).
 bool encode_tmap_2d(void* map, int dtype_code, void* base, uint64_t inner, uint64_t outer,

@@ -46,10 +46,23 @@ def _workload(name):
     if name == "k1":
         return synth.workload("custom", seed=13, q_lens=[257], ctx_lens=[0], num_q_heads=2,
                               num_kv_heads=1, head_dim=128, top_k=1)
+    if name == "quant_small":  # E4M3 Q, NVFP4 K/V (attention and indexer)
+        return synth.workload("custom", seed=15, q_lens=[300, 77], ctx_lens=[0, 1000],
+                              num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=5,
+                              q_dtype="e4m3", kv_dtype="nvfp4")
+    if name == "quant_d64":
+        return synth.workload("custom", seed=16, q_lens=[190], ctx_lens=[70], num_q_heads=2,
+                              num_kv_heads=1, head_dim=64, top_k=2, q_dtype="e4m3",
+                              kv_dtype="nvfp4")
+    if name == "chunked_fp8_small":  # chunked prefill, E4M3 indexer q/k, BF16 attention
+        return synth.workload("custom", seed=14, q_lens=[200, 64, 131], ctx_lens=[1000, 2900, 555],
+                              num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=6,
+                              idx_dtype="e4m3")
     return synth.workload(name, seed=0)
 
 
-SMALL = ["tiny", "ragged", "mha_d64", "k1"]
+SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64"]
+FULL = ["prefill8k", "prefill8k_q", "chunked32k"]
 _cache = {}
 
 
@@ -65,7 +78,7 @@ def _run(name):
     run.run_all()
     assert run.status() == 0
     full = w.num_rows <= 20000
-    rows = np.arange(w.num_rows, dtype=np.int64) if full else sample_rows(w, 384)
+    rows = np.arange(w.num_rows, dtype=np.int64) if full else sample_rows(w, 192)
     rows_t = torch.from_numpy(rows).to(run.dev)
     res = dict(
         w=w, t=t, run=run, rows=rows,
@@ -87,7 +100,7 @@ def _abs_tensor(tn: orc.Tensor) -> orc.Tensor:
     return orc.Tensor(data, tn.dtype, scales=tn.scales, scale=abs(tn.scale))
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_plan_metadata_bit_exact(name):
     r = _run(name)
     run, w = r["run"], r["w"]
@@ -98,7 +111,7 @@ def test_plan_metadata_bit_exact(name):
     assert np.array_equal(pos, opos) and np.array_equal(req, oreq)
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_indexer_scores(name):
     r = _run(name)
     w, rows = r["w"], r["rows"]
@@ -114,7 +127,7 @@ def test_indexer_scores(name):
     assert np.all(err <= tol), f"max err/tol {np.max(err / tol):.3g}"
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_topk_bit_exact_on_shared_scores(name):
     r = _run(name)
     w, rows = r["w"], r["rows"]
@@ -123,7 +136,7 @@ def test_topk_bit_exact_on_shared_scores(name):
     assert np.array_equal(r["idx"], ref)
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_forward_partials_and_lse(name):
     r = _run(name)
     w, rows = r["w"], r["rows"]
@@ -138,7 +151,7 @@ def test_forward_partials_and_lse(name):
     assert np.max(np.abs(got_l[filled] - lse[filled])) <= LSE_ATOL
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_output_matches_oracle(name):
     r = _run(name)
     w, rows = r["w"], r["rows"]
@@ -150,7 +163,7 @@ def test_output_matches_oracle(name):
     assert np.max(np.abs(r["out_lse"] - ref_lse)) <= LSE_ATOL
 
 
-@pytest.mark.parametrize("name", SMALL + ["prefill8k"])
+@pytest.mark.parametrize("name", SMALL + FULL)
 def test_inversion_bit_exact(name):
     r = _run(name)
     run, w = r["run"], r["w"]
@@ -298,3 +311,53 @@ def test_host_rejects_invalid_arguments():
     with pytest.raises(B.SpsError) as e:
         B.sps_plan_upload(run.plan, small_ws)
     assert e.value.status == 3
+
+
+def test_combine_stress_full_size():
+    """The combine-stress workload at full size: partial [16][16384*32][128] FP32 (4.3 GB) and
+    LSE ~ N(0, sd 2), generated on the device; sampled rows against the oracle."""
+    from paged_top_sparse_gb300 import binding as B
+
+    S, R, D = 16, 16384 * 32, 128
+    part, lse = synth.combine_inputs(R, S, D, seed=5, device="cuda:0")
+    lse[3, ::7] = float("-inf")  # some empty slots
+    out = torch.empty((R, D), dtype=torch.bfloat16, device="cuda:0")
+    out_lse = torch.empty(R, dtype=torch.float32, device="cuda:0")
+    B.partial_combine(part, lse, out, out_lse)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, 1, R - 1], rng.choice(R, 2000, replace=False)]))
+    rt = torch.from_numpy(rows).cuda()
+    ref, ref_lse = orc.combine(part[:, rt].cpu().numpy(), lse[:, rt].cpu().numpy())
+    got = out[rt].float().cpu().numpy()
+    assert rel_l2(got, ref) <= 2e-3 and np.max(np.abs(got - ref)) <= 1e-2
+    assert np.max(np.abs(out_lse[rt].cpu().numpy() - ref_lse)) <= LSE_ATOL
+    del part, lse
+
+
+def test_dequant_exhaustive_bit_exact():
+    """sps_dequantize against the oracle's decode: every E4M3 code, and every E2M1 code under
+    every E4M3 scale (NaN scales give NaN), bit for bit in FP16."""
+    from paged_top_sparse_gb300 import binding as B
+
+    codes = np.tile(np.arange(256, dtype=np.uint8), 16)
+    out = torch.empty(codes.size, dtype=torch.float16, device="cuda:0")
+    B.sps_dequantize("e4m3", torch.from_numpy(codes).cuda(), None, codes.size, out)
+    ref = orc.decode(orc.Tensor(codes, "e4m3"))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+    nib = np.tile(np.arange(16, dtype=np.uint8), 256)          # block b holds codes 0..15
+    packed = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    scales = np.arange(256, dtype=np.uint8)                     # block b has scale code b
+    out = torch.empty(nib.size, dtype=torch.float16, device="cuda:0")
+    B.sps_dequantize("nvfp4", torch.from_numpy(packed).cuda(), torch.from_numpy(scales).cuda(),
+                     nib.size, out)
+    ref = orc.decode(orc.Tensor(packed, "nvfp4", scales=scales))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
