@@ -96,6 +96,24 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(values, world: int):
+    """Element-wise maximum of per-rank timings over all ranks (identity on one rank)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, slowest_ms: float) -> float:
+    """Whole-job throughput: every rank processed its own batch within the slowest rank's time."""
+    return tokens_per_rank * world / (slowest_ms * 1e-3)
+
+
 def _algorithmic(w, idx_np):
     """Algorithmic bytes / FLOPs of each step for this batch (minimum traffic)."""
     R, K, D, H = w.num_rows, w.top_k, w.head_dim, w.num_q_heads
@@ -234,12 +252,7 @@ def run_gpu(args, rank, world):
     e2e_ms = float(np.mean(e_ms))
     clk = clocks.stop()
 
-    # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([step_ms, e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(tt[0]), float(tt[1])
+    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], world)
 
     alg = _algorithmic(w, idx.cpu().numpy())
     hbm, bf16, peak_kind = _peaks()
@@ -268,10 +281,9 @@ def run_gpu(args, rank, world):
             traffic = json.load(f).get(dom)
     except Exception:
         pass
-    tokens = w.num_tokens * world
     line = {
         "metric": METRIC,
-        "value": round(tokens / (step_ms * 1e-3), 1),
+        "value": round(job_tokens_per_s(w.num_tokens, world, step_ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -295,7 +307,7 @@ def run_gpu(args, rank, world):
         "kernels": kern,
         "combine_hbm_gbs": kern["combine"]["achieved"],
         "fwd_tensor_pipe_frac": kern["fwd"]["tensor_frac"],
-        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(w.num_tokens, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 9 * args.steps,

@@ -282,6 +282,16 @@ sps_status sparse_prefill_fwd_noalloc(const sps_plan* plan, const void* q, float
                                       sps_stream_t stream);
 
 /*
+ * sps_check_wait_timeout -- health check of the failure path every kernel relies on: a
+ * one-block kernel waits on an mbarrier that nothing ever arrives on, through the same bounded
+ * wait the pipelines use (their limit is 2 s; here `limit_ns`, 1 ms .. 10 s).  The wait gives
+ * up, records SPS_DEV_TIMEOUT in *dev_status (a device int32 the caller cleared) and the kernel
+ * returns; the context stays usable.  Asynchronous on `stream`.  ("MSA PR 36", Changes, notes a
+ * hang fixed in the indexer's K loader; here no wait can hang.)
+ */
+sps_status sps_check_wait_timeout(int64_t limit_ns, int32_t* dev_status, sps_stream_t stream);
+
+/*
  * sps_read_device_status -- synchronous: waits for the device, then copies the plan
  * workspace's status word into *code (SPS_DEV_*).  Returns SPS_EDEVICE when it is non-zero.
  */

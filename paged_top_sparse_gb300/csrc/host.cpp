@@ -470,6 +470,15 @@ sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales
                   "dequant launch");
 }
 
+sps_status sps_check_wait_timeout(int64_t limit_ns, int32_t* dev_status, sps_stream_t stream) {
+  if (!dev_status || !aligned(dev_status, 4))
+    return fail(SPS_EINVAL, "sps_check_wait_timeout: dev_status must be a device int32");
+  if (limit_ns < 1000000 || limit_ns > 10000000000LL)
+    return fail(SPS_EINVAL, "sps_check_wait_timeout: limit_ns must be in [1e6, 1e10]");
+  return launched(launch_wait_timeout(dev_status, limit_ns, reinterpret_cast<cudaStream_t>(stream)),
+                  "wait-timeout check launch");
+}
+
 sps_status sps_read_device_status(const sps_plan* pl, const void* ws, int32_t* code) {
   if (!code) return fail(SPS_EINVAL, "code is NULL");
   sps_status st = check_plan_ws(pl, ws);

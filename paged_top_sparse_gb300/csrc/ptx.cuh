@@ -68,14 +68,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // role already failed) or after kWaitLimitNs; on a timeout it raises DEV_TIMEOUT in the
 // status word and sets *abort.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         set_status(status, DEV_TIMEOUT);
         if (abort) *abort = 1;
         return false;

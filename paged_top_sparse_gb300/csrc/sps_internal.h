@@ -85,6 +85,9 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
                            int64_t split_stride, float* lse, int64_t lse_split_stride,
                            cudaStream_t st);
 
+// One-block kernel whose bounded wait on a never-arrived mbarrier must time out.
+cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t st);
+
 // Exact E4M3 / NVFP4 -> FP16 conversion of n elements (n % 16 == 0).
 cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
                            void* out, cudaStream_t st);

@@ -361,3 +361,26 @@ def test_dequant_exhaustive_bit_exact():
     assert np.array_equal(np.isnan(got), np.isnan(ref))
     ok = ~np.isnan(ref)
     assert np.array_equal(got[ok], ref[ok])
+
+
+def test_bounded_wait_times_out_without_hanging():
+    """A wait on an mbarrier that never completes ends after its limit with SPS_DEV_TIMEOUT in
+    the status word; the context stays usable for the next launch."""
+    import time
+
+    from paged_top_sparse_gb300 import binding as B
+
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    t0 = time.perf_counter()
+    B.sps_check_wait_timeout(200_000_000, st)  # 0.2 s
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == 1  # SPS_DEV_TIMEOUT
+    assert 0.15 < dt < 5.0
+    # the context still works
+    part = torch.randn((2, 64, 128), device="cuda:0")
+    lse = torch.zeros((2, 64), device="cuda:0")
+    out = torch.empty((64, 128), dtype=torch.bfloat16, device="cuda:0")
+    B.partial_combine(part, lse, out)
+    torch.cuda.synchronize()
+    assert torch.allclose(out.float(), part.mean(0), atol=2e-2)
