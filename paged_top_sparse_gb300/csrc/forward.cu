@@ -5,13 +5,16 @@
 // Only the row's own page is causally masked; K/V come through the page table.
 //
 // Design (GB300, one CTA per SM, persistent over the device-built work list):
-//   (warps 0-3 form the producer/MMA warpgroup, 4-7 the softmax, 8-11 the epilogue;
-//   setmaxnreg moves registers to the softmax)
+//   (warps 0-3 form the producer/MMA warpgroup, 4-7 the softmax, 8-11 the epilogue, 12-15 the
+//   Q gather; setmaxnreg moves registers to the softmax)
 //   warp 0     the K and V tiles of the item's physical page by TMA (128-byte swizzle);
-//   warp 2     per group the 128 query rows by TMA tile::gather4 into the same swizzled
-//              layout, in a 2-stage Q ring.  Every global access of the kernel's main loop
-//              runs on the TMA engine: gathering Q through the load/store unit instead left
-//              it queued behind the HBM-bound partial stores.
+//   warps 12-15 per group the 128 query rows by TMA tile::gather4 into the same swizzled
+//              layout, in a 2-stage Q ring.  A warp issues its gathers one lane after another,
+//              so the group's 64 gathers are spread over four warps (one per SM
+//              sub-partition); with one gathering warp the forward ran at its issue rate.
+//              Every global access of the kernel's main loop runs on the TMA engine:
+//              gathering Q through the load/store unit instead left it queued behind the
+//              HBM-bound partial stores.
 //   warp 1     MMA issuer (one thread): S = Q K^T (shared x shared, N = 128 keys) into a
 //              double-buffered TMEM accumulator, and O = P V with P read from TMEM (the
 //              softmax overwrites S with P in place) and V as an MN-major FP16 operand; it
@@ -24,8 +27,7 @@
 //              LSE = m * scale + ln l straight to global;
 //   warps 8-11 epilogue, a thread per row: O / l from TMEM into a padded staging row, then
 //              one bulk copy of the whole row into partial[slot][row].  The partial stores are
-//              bound by HBM; keeping them on the TMA engine leaves the load/store unit to the
-//              Q gather, which would otherwise queue behind them.
+//              bound by HBM; keeping them on the TMA engine leaves the load/store unit free.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,7 +39,7 @@ namespace {
 
 constexpr int kQS = 2;          // Q ring stages
 
-constexpr int kThreads = 384;   // 3 warpgroups
+constexpr int kThreads = 512;   // 4 warpgroups
 template <int D>
 constexpr int stage_pitch() { return D + 4; }  // floats per staging row (pad: conflict-free)
 
@@ -87,7 +89,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
     mbar_init(smem_u32(&sm.kv_empty), 1);
     mbar_init(smem_u32(&sm.v_ready), 4);
     for (int i = 0; i < kQS; ++i) {
-      mbar_init(smem_u32(&sm.q_full[i]), 1);
+      mbar_init(smem_u32(&sm.q_full[i]), 4);  // one arrival per gather warp
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -113,10 +115,10 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   const uint32_t tmem = sm.tmem_base;  // S[b] at column 128 b, O[b] at 256 + 128 b
   volatile int* abort_flag = &sm.abort_flag;
 
-  // Registers: the block launches with 168 per thread (384 x 168 = 64512); the producer/MMA
-  // warpgroup gives part of its share to the softmax warpgroup, which holds a whole S row
-  // ((96 + 232 + 168) x 128 = 63488).  Each role's code sits under its own setmaxnreg so the
-  // compiler allocates it within that budget.
+  // Registers: the block launches with 128 per thread (512 x 128 = 65536); the producer/MMA
+  // and gather warpgroups give part of their share to the softmax warpgroup, which holds a
+  // whole S row ((96 + 232 + 128 + 56) x 128 = 65536).  Each role's code sits under its own
+  // setmaxnreg so the compiler allocates it within that budget.
   if (warp < 4) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
   if (warp == 0) {
@@ -142,52 +144,6 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
         tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, f);
       }
       ++kv_it;
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------ Q gather (TMA tile::gather4)
-    // Lane l gathers group rows 4l .. 4l+3 (rows past the end of the group repeat its first
-    // row) into the 128-byte-swizzled K-major tile, one gather4 per 64-column block; the
-    // indices of group g+1 are fetched while g is issued.
-    const uint64_t pol_q = l2_policy_evict_last();  // Q rows are re-read once per page
-    uint32_t q_it = 0;
-    bool ok = true;
-    for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
-      const FwdTask t = p.fwd_tasks[ti];
-      const int ngroups = (t.count + 127) / 128;
-      auto fetch_rows = [&](int grp, int (&rows)[4]) {
-        const int base = t.entry_begin + grp * 128;
-        const int n_in = min(128, t.count - grp * 128);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = 4 * lane + j;
-          rows[j] = __ldg(&p.entries[base + (i < n_in ? i : 0)].x);
-        }
-      };
-      int nxt[4];
-      fetch_rows(0, nxt);
-      for (int grp = 0; grp < ngroups; ++grp) {
-        int rows[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rows[j] = nxt[j];
-          if (rows[j] < 0 || rows[j] >= R) {
-            set_status(status, DEV_OVERFLOW);
-            rows[j] = 0;
-          }
-        }
-        if (grp + 1 < ngroups) fetch_rows(grp + 1, nxt);
-        const int qs = q_it % kQS;
-        const uint32_t qf = smem_u32(&sm.q_full[qs]);
-        if (lane == 0) {
-          ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
-          if (ok) mbar_expect_tx(qf, TILE);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        for (int db = 0; db < DB; ++db)
-          tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + lane * 512, &tmQ, db * 64, rows[0],
-                           rows[1], rows[2], rows[3], qf, pol_q);
-        ++q_it;
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (one thread)
@@ -389,7 +345,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       }
       if (!ok) break;
     }
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------ epilogue: warps 8..11
     // A thread per row: O / l from TMEM into its padded staging row, then one bulk copy of
     // the whole row (D x 4 bytes) into partial[slot][row].  The stores run on the TMA engine,
@@ -449,6 +405,59 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       }
     }
     bulk_wait_all<0>();
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    // ------------------------------------------------ Q gather (TMA tile::gather4): warps 12..15
+    // A group's 32 DB gather4 operations (4 rows x one 64-column block each) are spread over
+    // the four warps, one per SM sub-partition: lane l < 8 DB of warp w issues operation
+    // op = 8 DB w + l, column block op / 32, group rows 4 (op % 32) .. +3 (rows past the end
+    // of the group repeat its first row).  The indices of group g+1 are fetched while g is
+    // issued.
+    const int nops = 8 * DB;
+    const int op = (warp - 12) * nops + lane;
+    const int db = op / 32, quad = op % 32;
+    const bool active = lane < nops;
+    const uint64_t pol_q = l2_policy_evict_last();  // Q rows are re-read once per page
+    uint32_t q_it = 0;
+    bool ok = true;
+    for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
+      const FwdTask t = p.fwd_tasks[ti];
+      const int ngroups = (t.count + 127) / 128;
+      auto fetch_rows = [&](int grp, int (&rows)[4]) {
+        const int base = t.entry_begin + grp * 128;
+        const int n_in = min(128, t.count - grp * 128);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * quad + j;
+          rows[j] = active ? __ldg(&p.entries[base + (i < n_in ? i : 0)].x) : 0;
+        }
+      };
+      int nxt[4];
+      fetch_rows(0, nxt);
+      for (int grp = 0; grp < ngroups; ++grp) {
+        int rows[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          rows[j] = nxt[j];
+          if (rows[j] < 0 || rows[j] >= R) {
+            set_status(status, DEV_OVERFLOW);
+            rows[j] = 0;
+          }
+        }
+        if (grp + 1 < ngroups) fetch_rows(grp + 1, nxt);
+        const int qs = q_it % kQS;
+        const uint32_t qf = smem_u32(&sm.q_full[qs]);
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
+          if (ok) mbar_expect_tx(qf, TILE / 4);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (active)
+          tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + quad * 512, &tmQ, db * 64, rows[0],
+                           rows[1], rows[2], rows[3], qf, pol_q);
+        ++q_it;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -5,10 +5,12 @@
 // n_sel - 1 = min(k, o+1) - 1 pages are the best by (score descending, page ascending), with
 // -0.0 equal to +0.0; output in ascending page order, padded with -1.
 //
-// Each lane holds pages lane, lane+32, ... as 32-bit order-preserving keys of their scores.
-// A selection round is two warp reductions (redux.sync): the maximum key, then the lowest
-// page among the lanes that hold it; the winner is marked taken.  n_sel - 1 rounds, then a
-// ballot/popc prefix writes the chosen pages in ascending order.
+// Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
+// sorted best-first once (bitonic network in registers), so any page of a lower lane is lower
+// than every page of a higher lane.  A selection round is then one warp max-reduction
+// (redux.sync) of the lanes' head keys and one ballot: the lowest lane whose head holds the
+// maximum has the winning page (ties go to the lower page) and shifts its next candidate up.
+// After n_sel - 1 rounds a ballot/popc prefix writes the chosen pages in ascending order.
 #include "ptx.cuh"
 #include "sps_internal.h"
 
@@ -22,6 +24,27 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Sorts a lane's E candidates (key, page offset) best-first: larger key, then lower page.
+template <int E>
+__device__ __forceinline__ void sort_best_first(uint32_t (&k)[E], uint32_t (&pg)[E]) {
+#pragma unroll
+  for (int size = 2; size <= E; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int l = i ^ stride;
+        if (l > i) {
+          const bool l_better = k[l] > k[i] || (k[l] == k[i] && pg[l] < pg[i]);
+          if (l_better == ((i & size) == 0)) {  // best-first runs where bit `size` of i is 0
+            const uint32_t tk = k[i], tp = pg[i];
+            k[i] = k[l]; pg[i] = pg[l];
+            k[l] = tk; pg[l] = tp;
+          }
+        }
+      }
+}
+
 template <int E>  // pages per lane: max_pages <= 32 * E
 __global__ void __launch_bounds__(256)
 topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t* __restrict__ idx) {
@@ -29,52 +52,52 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t R = (int64_t)p.T * p.H;
   if (r >= R) return;
-  const int tok = (int)(r / p.H);
-  const int t = __ldg(p.tok_pos + tok);
-  const int o = t >> 7;
-  const int n = o + 1;
-  const int K = p.K;
+  const int o = __ldg(p.tok_pos + r / p.H) >> 7;
+  const int n = o + 1, K = p.K;
   int32_t* out = idx + r * K;
   if (n <= K) {  // every visible page is kept
     for (int s = lane; s < K; s += 32) out[s] = s < n ? s : -1;
     return;
   }
   const float* row = scores + r * pitch;
-  uint32_t key[E];
+  const int base = lane * E;
+  uint32_t key[E], pg[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
-    int pg = lane + 32 * j;
-    key[j] = (pg < n && pg != o) ? score_key(__ldg(row + pg)) : 0u;
+    const int page = base + j;
+    pg[j] = (uint32_t)j;
+    key[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
   }
-  uint32_t taken = 0;  // bit j: page lane + 32 j selected
+  sort_best_first<E>(key, pg);
+  const uint32_t lt = (1u << lane) - 1u;
+  int c = 0;  // this lane's candidates taken so far: the first c of the sorted order
+#pragma unroll 4
   for (int round = 1; round < K; ++round) {
-    // best remaining key of this lane; equal keys keep the lower page (lower j)
-    uint32_t bk = 0;
-    int bj = 0;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t tie = __ballot_sync(0xffffffffu, key[0] == m);
+    if (key[0] == m && (tie & lt) == 0) {
+      ++c;
 #pragma unroll
-    for (int j = 0; j < E; ++j)
-      if (key[j] > bk) { bk = key[j]; bj = j; }
-    const uint32_t wmax = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = (bk == wmax) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
-    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-    if ((int)(win & 31) == lane) {
-      const int wj = (int)(win >> 5);
-#pragma unroll
-      for (int j = 0; j < E; ++j)
-        if (j == wj) { taken |= 1u << j; key[j] = 0u; }
+      for (int j = 0; j + 1 < E; ++j) key[j] = key[j + 1];
+      key[E - 1] = 0u;
     }
   }
-  if ((o & 31) == lane) taken |= 1u << (o >> 5);
-  // ascending output through ballot prefix counts
-  int before = 0;
-  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t taken = 0;  // bit j: page base + j selected
 #pragma unroll
-  for (int j = 0; j < E; ++j) {
-    const uint32_t bal = __ballot_sync(0xffffffffu, (taken >> j) & 1u);
-    if ((taken >> j) & 1u) out[before + __popc(bal & lt)] = lane + 32 * j;
-    before += __popc(bal);
+  for (int j = 0; j < E; ++j)
+    if (j < c) taken |= 1u << pg[j];
+  if (o / E == lane) taken |= 1u << (o % E);
+  // ascending output: pages before this lane's are those of lower lanes
+  int before = __popc(taken);
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, before, d);
+    if (lane >= d) before += y;
   }
-  // before == K here (n > K): no padding needed
+  before -= __popc(taken);
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if ((taken >> j) & 1u) out[before++] = base + j;
 }
 
 }  // namespace

@@ -136,6 +136,41 @@ def test_topk_bit_exact_on_shared_scores(name):
     assert np.array_equal(r["idx"], ref)
 
 
+@pytest.mark.parametrize("q_lens,ctx_lens,k", [
+    ([1024], [0], 4),            # 8 pages
+    ([601, 334], [4500, 0], 16),  # up to 41 pages, two requests, ragged rows
+    ([500], [7600], 16),          # 64 pages
+    ([256], [12000], 7),          # 96 pages
+    ([64], [20000], 16),          # 157 pages
+    ([200], [3000], 32),          # 25 pages, k above the page count for most rows
+    ([130], [38000], 64),         # 298 pages, the largest k
+])
+def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
+    """Scores drawn from {-1.5, ..., 1.5} with signed zeros: most pages tie with others, so
+    the (score desc, page asc) order and -0.0 == +0.0 decide most selections."""
+    from paged_top_sparse_gb300 import binding as B
+
+    w = synth.workload("custom", seed=21, q_lens=q_lens, ctx_lens=ctx_lens, num_q_heads=4,
+                       num_kv_heads=2, head_dim=128, top_k=k)
+    plan = B.Plan(w.q_lens, w.ctx_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.top_k,
+                  w.max_pages, w.num_phys_pages)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda:0")
+    B.sps_plan_upload(plan, ws)
+    rng = np.random.default_rng(5)
+    R, P = w.num_rows, w.max_pages
+    s = (rng.integers(-3, 4, size=(R, P)) * 0.5).astype(np.float32)
+    s[rng.random((R, P)) < 0.2] = -0.0
+    s[:7] = 1.0  # whole rows of equal scores
+    _, tok_pos = orc.token_meta(oracle_problem(w))
+    own = (tok_pos[np.arange(R) // w.num_q_heads] // 128)[:, None]
+    s[np.arange(P)[None, :] > own] = np.nan  # never read by the selection
+    idx = torch.full((R, k), -7, dtype=torch.int32, device="cuda:0")
+    B.topk_select(plan, torch.from_numpy(s).cuda(), idx, ws)
+    torch.cuda.synchronize()
+    ref = orc.topk(oracle_problem(w), np.nan_to_num(s.astype(np.float64), nan=-np.inf))
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("name", SMALL + FULL)
 def test_forward_partials_and_lse(name):
     r = _run(name)
