@@ -9,7 +9,9 @@
 //     [T][H][D], 128-byte swizzle) into a 2-stage Q ring; per page, the physical K tile
 //     (looked up in the page table) into a 3-stage K ring;
 //   * warp 1 (MMA issuer, one thread): S_h = Q_h K^T, M = 128 rows, N = 128 keys, FP32
-//     accumulators in TMEM, double-buffered per head (4 x 128 columns);
+//     accumulators in TMEM, double-buffered per head (4 x 128 columns).  The two heads' K
+//     steps are issued interleaved from descriptors built once per tile: a single thread has
+//     to issue an MMA every ~64 cycles to keep the tensor core busy, so the loop stays short;
 //   * warps 2-9 (epilogue, one warpgroup per head, a thread per row): the per-page row max
 //     comes straight out of TMEM with tcgen05.ld.red.max; only rows whose own page it is take
 //     the element-wise masked path (a warp-uniform vote picks the path).
@@ -130,6 +132,8 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int qs = q_it % kQStages;
         if (!mbar_wait(smem_u32(&sm.q_full[qs]), (q_it / kQStages) & 1, abort_flag, status)) break;
         bool ok = true;
+        const uint64_t ad0 = sdesc_sw128(smem_u32(sm.q[qs][0]), 16, 1024);
+        const uint64_t ad1 = sdesc_sw128(smem_u32(sm.q[qs][1]), 16, 1024);
         for (int pg = t.page_begin; pg < t.page_end; ++pg) {
           const int ks = k_it % kKStages;
           const int ab = a_it & 1;
@@ -139,17 +143,27 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint32_t kbase = smem_u32(sm.k[ks]);
-          for (int h = 0; h < t.nh; ++h) {
-            const uint32_t qbase = smem_u32(sm.q[qs][h]);
-            const uint32_t d_tmem = tmem + (uint32_t)((ab * 2 + h) * 128);
+          // descriptors built once; a K step only moves the start address (16-byte units)
+          const uint64_t bd0 = sdesc_sw128(smem_u32(sm.k[ks]), 16, 1024);
+          const uint32_t d0 = tmem + (uint32_t)(ab * 256);
+          if (t.nh == 2) {
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
-              const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-              const uint64_t ad = sdesc_sw128(qbase + off, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kbase + off, 16, 1024);
-              if (FP8) mma_f8_ss(d_tmem, ad, bd, IDESC, kk > 0);
-              else mma_f16_ss(d_tmem, ad, bd, IDESC, kk > 0);
+              const uint64_t off = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+              if (FP8) {
+                mma_f8_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
+                mma_f8_ss(d0 + 128, ad1 + off, bd0 + off, IDESC, kk > 0);
+              } else {
+                mma_f16_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
+                mma_f16_ss(d0 + 128, ad1 + off, bd0 + off, IDESC, kk > 0);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+              const uint64_t off = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+              if (FP8) mma_f8_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
+              else mma_f16_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
             }
           }
           mma_commit(smem_u32(&sm.k_empty[ks]));
