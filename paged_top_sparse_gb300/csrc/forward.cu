@@ -7,24 +7,26 @@
 // Design (GB300, one CTA per SM, persistent over the device-built work list):
 //   (warps 0-3 form the producer/MMA warpgroup, 4-7 the softmax, 8-11 the epilogue, 12-15 the
 //   Q gather; setmaxnreg moves registers to the softmax)
-//   warp 0     the K and V tiles of the item's physical page by TMA (128-byte swizzle);
+//   warp 0     the K and V tiles of the item's physical page by TMA (128-byte swizzle), with
+//              separate barriers: the next item's K loads as soon as the last S of the
+//              current item has read the old tile, its V after the last P.V;
+//   warps 2-3  convert the V tile BF16 -> FP16 in place once per item;
 //   warps 12-15 per group the 128 query rows by TMA tile::gather4 into the same swizzled
 //              layout, in a 2-stage Q ring.  A warp issues its gathers one lane after another,
 //              so the group's 64 gathers are spread over four warps (one per SM
-//              sub-partition); with one gathering warp the forward ran at its issue rate.
-//              Every global access of the kernel's main loop runs on the TMA engine:
-//              gathering Q through the load/store unit instead left it queued behind the
-//              HBM-bound partial stores.
+//              sub-partition); the row indices of the next group (across item boundaries)
+//              are loaded while the current one is issued.  Every global access of the main
+//              loop runs on the TMA engine: gathering Q through the load/store unit instead
+//              left it queued behind the HBM-bound partial stores.
 //   warp 1     MMA issuer (one thread): S = Q K^T (shared x shared, N = 128 keys) into a
 //              double-buffered TMEM accumulator, and O = P V with P read from TMEM (the
 //              softmax overwrites S with P in place) and V as an MN-major FP16 operand; it
 //              polls both streams and issues whichever is ready, so S of group g+1 overlaps
 //              the softmax of group g without a late Q tile delaying P.V of group g;
-//   warps 4-7  softmax, a thread per row: converts the V tile BF16 -> FP16 in place once per
-//              item; per group, one TMEM read of the row (tcgen05.ld.red.max gives the max
-//              unless some lane of the warp owns the page, then the masked element-wise
-//              path), p = 2^(s c - m c) rounded to FP16 back into TMEM over S, l = sum p,
-//              LSE = m * scale + ln l straight to global;
+//   warps 4-7  softmax, a thread per row: per group, one TMEM read of the row
+//              (tcgen05.ld.red.max gives the max unless some lane of the warp owns the page,
+//              then the masked element-wise path), p = 2^(s c - m c) rounded to FP16 back into
+//              TMEM over S, l = sum p, LSE = m * scale + ln l straight to global;
 //   warps 8-11 epilogue, a thread per row: O / l from TMEM into a padded staging row, then
 //              one bulk copy of the whole row into partial[slot][row].  The partial stores are
 //              bound by HBM; keeping them on the TMA engine leaves the load/store unit free.
@@ -52,7 +54,7 @@ struct FwdSmem {
   float stage[128 * stage_pitch<D>()];  // one O row per epilogue thread
   float inv_l[2][128];
   int2 rs[2][128];
-  uint64_t kv_full, kv_empty, v_ready;
+  uint64_t k_full, k_empty, v_full, v_empty, v_ready;
   uint64_t q_full[kQS], q_empty[kQS];
   uint64_t s_full[2], p_full[2], s_free[2], o_full[2], o_empty[2], st_full[2], st_empty[2];
   uint64_t done;
@@ -85,9 +87,11 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   const int64_t R = (int64_t)p.T * p.H;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&sm.kv_full), 1);
-    mbar_init(smem_u32(&sm.kv_empty), 1);
-    mbar_init(smem_u32(&sm.v_ready), 4);
+    mbar_init(smem_u32(&sm.k_full), 1);
+    mbar_init(smem_u32(&sm.k_empty), 1);
+    mbar_init(smem_u32(&sm.v_full), 1);
+    mbar_init(smem_u32(&sm.v_empty), 1);
+    mbar_init(smem_u32(&sm.v_ready), 2);  // the two V-conversion warps
     for (int i = 0; i < kQS; ++i) {
       mbar_init(smem_u32(&sm.q_full[i]), 4);  // one arrival per gather warp
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
@@ -130,19 +134,23 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       const int gp = t.bucket / p.Hkv, g = t.bucket % p.Hkv;
       const int req = p.page_req[gp];
       const int pg = gp - p.reqs[req].page_base;
-      if (!mbar_wait(smem_u32(&sm.kv_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
       int phys = __ldg(page_table + (int64_t)req * p.max_pages + pg);
       if (phys < 0 || phys >= p.num_phys) {
         set_status(status, DEV_BAD_PAGE);
         phys = 0;
       }
-      const uint32_t f = smem_u32(&sm.kv_full);
-      mbar_expect_tx(f, 2 * TILE);
       const int krow = (phys * p.Hkv + g) * 128;
-      for (int db = 0; db < DB; ++db) {
-        tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * 64, krow, f);
-        tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, f);
-      }
+      // K as soon as the previous item's last S has read the old tile, V after its last P.V
+      if (!mbar_wait(smem_u32(&sm.k_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
+      const uint32_t kf = smem_u32(&sm.k_full);
+      mbar_expect_tx(kf, TILE);
+      for (int db = 0; db < DB; ++db)
+        tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * 64, krow, kf);
+      if (!mbar_wait(smem_u32(&sm.v_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
+      const uint32_t vf = smem_u32(&sm.v_full);
+      mbar_expect_tx(vf, TILE);
+      for (int db = 0; db < DB; ++db)
+        tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, vf);
       ++kv_it;
     }
   } else if (warp == 1) {
@@ -153,8 +161,11 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
     if (lane == 0) {
       // S cursor (task ti_s, group grp_s) and P.V cursor (ti_p, grp_p); gs / gp count groups
       int ti_s = blockIdx.x, grp_s = 0, ti_p = blockIdx.x, grp_p = 0;
-      int ng_s = ti_s < ntasks ? (p.fwd_tasks[ti_s].count + 127) / 128 : 0;
+      auto ngroups_of = [&](int ti) { return ti < ntasks ? (p.fwd_tasks[ti].count + 127) / 128 : 0; };
+      int ng_s = ngroups_of(ti_s);
       int ng_p = ng_s;
+      // group counts of the following items, loaded ahead of the item switch
+      int ng_s_next = ngroups_of(ti_s + gridDim.x), ng_p_next = ng_s_next;
       uint32_t gs = 0, gp = 0, q_it = 0, kv_s = 0, kv_p = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
@@ -176,11 +187,12 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
             mma_commit(smem_u32(&sm.o_full[b]));
             ++gp;
             if (++grp_p == ng_p) {  // the item's last P.V: its K/V tiles may be replaced
-              mma_commit(smem_u32(&sm.kv_empty));
+              mma_commit(smem_u32(&sm.v_empty));
               ++kv_p;
               grp_p = 0;
               ti_p += gridDim.x;
-              ng_p = ti_p < ntasks ? (p.fwd_tasks[ti_p].count + 127) / 128 : 0;
+              ng_p = ng_p_next;
+              ng_p_next = ngroups_of(ti_p + gridDim.x);
             }
             progressed = true;
           }
@@ -188,7 +200,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
         if (ti_s < ntasks && gs < gp + 2) {  // S(gs)
           const int qs = q_it % kQS;
           const int b = gs & 1;
-          if ((grp_s != 0 || mbar_try_wait(smem_u32(&sm.kv_full), kv_s & 1)) &&
+          if ((grp_s != 0 || mbar_try_wait(smem_u32(&sm.k_full), kv_s & 1)) &&
               mbar_try_wait(smem_u32(&sm.q_full[qs]), (q_it / kQS) & 1) &&
               mbar_try_wait(smem_u32(&sm.s_free[b]), ((gs >> 1) & 1) ^ 1)) {
             tc_fence_after();
@@ -203,11 +215,13 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
             mma_commit(smem_u32(&sm.q_empty[qs]));
             ++q_it;
             ++gs;
-            if (++grp_s == ng_s) {
+            if (++grp_s == ng_s) {  // the item's last S: its K tile may be replaced
+              mma_commit(smem_u32(&sm.k_empty));
               ++kv_s;
               grp_s = 0;
               ti_s += gridDim.x;
-              ng_s = ti_s < ntasks ? (p.fwd_tasks[ti_s].count + 127) / 128 : 0;
+              ng_s = ng_s_next;
+              ng_s_next = ngroups_of(ti_s + gridDim.x);
             }
             progressed = true;
           }
@@ -227,25 +241,15 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       mma_commit(smem_u32(&sm.done));
       mbar_wait(smem_u32(&sm.done), 0, nullptr, status);
     }
-  }
-  } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
-    // ------------------------------------------------ softmax: warps 4..7
-    const int quarter = warp % 4;
-    const int row = quarter * 32 + lane;
-    const int sm_tid = (warp - 4) * 32 + lane;
-    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const float c = p.sm_scale * q_scale * 1.4426950408889634f;  // scale * log2(e)
-    uint32_t kv_it = 0, g_it = 0;
+  } else {
+    // ------------------------------------------------ V tile BF16 -> FP16 in place: warps 2, 3
+    const int ct = (warp - 2) * 32 + lane;
+    uint32_t kv_it = 0;
     for (int ti = blockIdx.x; ti < ntasks; ti += gridDim.x) {
-      const FwdTask t = p.fwd_tasks[ti];
-      const int gp = t.bucket / p.Hkv;
-      const int pg = gp - p.reqs[p.page_req[gp]].page_base;
-      // V tile: BF16 -> FP16 in place (same swizzled positions)
-      if (!mbar_wait(smem_u32(&sm.kv_full), kv_it & 1, abort_flag, status)) break;
+      if (!mbar_wait(smem_u32(&sm.v_full), kv_it & 1, abort_flag, status)) break;
       if (!F16IN) {
         uint4* v4 = reinterpret_cast<uint4*>(sm.v);
-        for (int i = sm_tid; i < TILE / 16; i += 128) {
+        for (int i = ct; i < TILE / 16; i += 64) {
           uint4 x = v4[i];
           uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -262,6 +266,20 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.v_ready));
       ++kv_it;
+    }
+  }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    // ------------------------------------------------ softmax: warps 4..7
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const float c = p.sm_scale * q_scale * 1.4426950408889634f;  // scale * log2(e)
+    uint32_t g_it = 0;
+    for (int ti = blockIdx.x; ti < ntasks; ti += gridDim.x) {
+      const FwdTask t = p.fwd_tasks[ti];
+      const int gp = t.bucket / p.Hkv;
+      const int pg = gp - p.reqs[p.page_req[gp]].page_base;
       const int ngroups = (t.count + 127) / 128;
       bool ok = true;
       // this thread's entry of group g+1 is loaded while group g is processed
@@ -420,43 +438,56 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
     const uint64_t pol_q = l2_policy_evict_last();  // Q rows are re-read once per page
     uint32_t q_it = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ti < ntasks && ok; ti += gridDim.x) {
-      const FwdTask t = p.fwd_tasks[ti];
-      const int ngroups = (t.count + 127) / 128;
-      auto fetch_rows = [&](int grp, int (&rows)[4]) {
-        const int base = t.entry_begin + grp * 128;
-        const int n_in = min(128, t.count - grp * 128);
+    auto fetch_rows = [&](const FwdTask& tk, int grp, int (&rows)[4]) {
+      const int base = tk.entry_begin + grp * 128;
+      const int n_in = min(128, tk.count - grp * 128);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = 4 * quad + j;
-          rows[j] = active ? __ldg(&p.entries[base + (i < n_in ? i : 0)].x) : 0;
-        }
-      };
-      int nxt[4];
-      fetch_rows(0, nxt);
-      for (int grp = 0; grp < ngroups; ++grp) {
-        int rows[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rows[j] = nxt[j];
-          if (rows[j] < 0 || rows[j] >= R) {
-            set_status(status, DEV_OVERFLOW);
-            rows[j] = 0;
-          }
-        }
-        if (grp + 1 < ngroups) fetch_rows(grp + 1, nxt);
-        const int qs = q_it % kQS;
-        const uint32_t qf = smem_u32(&sm.q_full[qs]);
-        if (lane == 0) {
-          ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
-          if (ok) mbar_expect_tx(qf, TILE / 4);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (active)
-          tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + quad * 512, &tmQ, db * 64, rows[0],
-                           rows[1], rows[2], rows[3], qf, pol_q);
-        ++q_it;
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * quad + j;
+        rows[j] = active ? __ldg(&p.entries[base + (i < n_in ? i : 0)].x) : 0;
       }
+    };
+    // groups of this CTA's items in order; the row indices (and, across an item boundary, the
+    // next item's descriptor) of group n+1 are loaded while group n is issued
+    int ti = blockIdx.x, grp = 0;
+    FwdTask t;
+    int nxt[4];
+    if (ti < ntasks) {
+      t = p.fwd_tasks[ti];
+      fetch_rows(t, 0, nxt);
+    }
+    while (ti < ntasks && ok) {
+      int rows[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        rows[j] = nxt[j];
+        if (rows[j] < 0 || rows[j] >= R) {
+          set_status(status, DEV_OVERFLOW);
+          rows[j] = 0;
+        }
+      }
+      int ti2 = ti, grp2 = grp + 1;
+      FwdTask t2 = t;
+      if (grp2 * 128 >= t.count) {
+        ti2 = ti + gridDim.x;
+        grp2 = 0;
+        if (ti2 < ntasks) t2 = p.fwd_tasks[ti2];
+      }
+      if (ti2 < ntasks) fetch_rows(t2, grp2, nxt);
+      const int qs = q_it % kQS;
+      const uint32_t qf = smem_u32(&sm.q_full[qs]);
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
+        if (ok) mbar_expect_tx(qf, TILE / 4);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (active)
+        tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + quad * 512, &tmQ, db * 64, rows[0],
+                         rows[1], rows[2], rows[3], qf, pol_q);
+      ++q_it;
+      ti = ti2;
+      grp = grp2;
+      t = t2;
     }
   }
   tc_fence_before();
