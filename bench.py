@@ -114,7 +114,7 @@ def job_tokens_per_s(tokens_per_rank: int, world: int, slowest_ms: float) -> flo
     return tokens_per_rank * world / (slowest_ms * 1e-3)
 
 
-def _algorithmic(w, idx_np):
+def _algorithmic(w, idx_np, partial_bytes=4):
     """Algorithmic bytes / FLOPs of each step for this batch (minimum traffic)."""
     R, K, D, H = w.num_rows, w.top_k, w.head_dim, w.num_q_heads
     tok_pos = np.concatenate([c + np.arange(q) for q, c in zip(w.q_lens, w.ctx_lens)])
@@ -137,9 +137,9 @@ def _algorithmic(w, idx_np):
                          + int((o + 1).sum()) * 4,
         "topk_bytes": int((o + 1).sum()) * 4 + R * K * 4,
         "fwd_flops": 4.0 * D * sel_keys,
-        "fwd_bytes": filled * D * 4 + R * K * 4 + R * D * (1 if w.q_dtype == "e4m3" else 2)
+        "fwd_bytes": filled * D * partial_bytes + R * K * 4 + R * D * (1 if w.q_dtype == "e4m3" else 2)
                      + kv_bytes + R * K * 4,
-        "combine_bytes": filled * D * 4 + R * K * 4 + R * D * 2 + R * 4,
+        "combine_bytes": filled * D * partial_bytes + R * K * 4 + R * D * 2 + R * 4,
         "filled_slots": filled,
     }
 
@@ -272,11 +272,14 @@ def run_gpu(args, rank, world):
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     scores = torch.empty((R, w.max_pages), dtype=torch.float32, device=dev)
     idx = torch.empty((R, K), dtype=torch.int32, device=dev)
-    partial = torch.empty((K, R, D), dtype=torch.float32, device=dev)
+    bf16p = args.partials == "bf16"
+    partial = torch.empty((K, R, D), dtype=torch.bfloat16 if bf16p else torch.float32, device=dev)
     lse = torch.empty((K, R), dtype=torch.float32, device=dev)
     out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    fwd_call = B.sparse_prefill_fwd_bf16 if bf16p else B.sparse_prefill_fwd
+    combine_call = B.partial_combine_bf16 if bf16p else B.partial_combine
 
     def step(ev, di=din):
         pl = B.Plan(*plan_args, **plan_kw)
@@ -291,10 +294,10 @@ def run_gpu(args, rank, world):
         if ev: ev[1].record(stream)
         B.topk_select(pl, scores, idx, ws)
         if ev: ev[2].record(stream)
-        B.sparse_prefill_fwd(pl, di["q"], q_scale, di["k"], di["v"], di.get("k_scales"),
-                             di.get("v_scales"), di["pt"], idx, partial, lse, ws)
+        fwd_call(pl, di["q"], q_scale, di["k"], di["v"], di.get("k_scales"),
+                 di.get("v_scales"), di["pt"], idx, partial, lse, ws)
         if ev: ev[3].record(stream)
-        B.partial_combine(partial, lse, out)
+        combine_call(partial, lse, out)
         if ev: ev[4].record(stream)
         return pl
 
@@ -318,7 +321,7 @@ def run_gpu(args, rank, world):
 
     step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], world)
 
-    alg = _algorithmic(w, idx.cpu().numpy())
+    alg = _algorithmic(w, idx.cpu().numpy(), partial_bytes=2 if bf16p else 4)
     hbm, bf16, peak_kind = _peaks()
     idx_peak = bf16 * 2 if idx_fp8 else bf16  # FP8 tensor rate: the nominal 2x of BF16
     k_ms = per.mean(0)
@@ -341,7 +344,7 @@ def run_gpu(args, rank, world):
     kern["fwd"]["tensor_frac"] = round(kern["fwd"]["tensor_tflops"] / bf16, 4)
     dom = names[int(np.argmax(k_ms))]
     traffic = None
-    if args.workload == "prefill8k" and args.tokens == 8192:  # counters taken on this workload
+    if args.workload == "prefill8k" and args.tokens == 8192 and not bf16p:  # counters' workload
         try:
             with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
                 traffic = json.load(f).get(dom)
@@ -361,7 +364,8 @@ def run_gpu(args, rank, world):
         "dtype": "fp16" if w.kv_dtype == "nvfp4" else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, quantised where the workload says; permuted "
                 "page table)",
-        "config": {"workload": _describe(w, args.workload),
+        "config": {"workload": _describe(w, args.workload) + (", BF16 partials" if bf16p else ""),
+                   "partials": "bf16" if bf16p else "fp32",
                    "batch": int(w.batch), "seq_len": int(max(w.q_lens)), "rows": int(R),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (256 MB write); per-step CUDA events"},
@@ -527,6 +531,9 @@ def main():
     ap.add_argument("--workload", default="prefill8k", choices=WORKLOADS,
                     help="prefill8k (default: the headline line), prefill8k_q (E4M3 Q, NVFP4 "
                          "K/V), chunked32k (8 x 512 over 32K context), combine_stress")
+    ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
+                    help="partial storage: fp32 (the contract; default) or bf16 (the pages' "
+                         "storage, sparse_prefill_fwd_bf16 + partial_combine_bf16)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))

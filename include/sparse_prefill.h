@@ -230,6 +230,28 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
                            int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sparse_prefill_fwd_bf16 / partial_combine_bf16 -- the same two steps with the partial
+ * outputs stored as BF16, the storage the pages keep ("MSA PR 21", Combine: keep BF16/FP16
+ * partials and outputs only).  It halves the forward's writes and the combine's reads.
+ *   partial_bf16  device BF16; element (s, r, d) at partial_bf16[s * split_stride + r * D + d]
+ *                 (elements); 16-byte aligned, split_stride a multiple of 8 and >= rows * D
+ * Every other argument, the LSE and the output are those of sparse_prefill_fwd and
+ * partial_combine.  The forward rounds each normalised partial to BF16 (round to nearest
+ * even); the combine widens them exactly to FP32 and accumulates in FP32.
+ */
+sps_status sparse_prefill_fwd_bf16(const sps_plan* plan, const void* q, float q_scale,
+                                   const void* k_cache, const void* v_cache,
+                                   const void* k_scales, const void* v_scales,
+                                   const int32_t* page_table, const int32_t* idx,
+                                   void* partial_bf16, int64_t split_stride, float* lse,
+                                   int64_t lse_split_stride, void* workspace,
+                                   sps_stream_t stream);
+sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
+                                const void* partial_bf16, int64_t split_stride, const float* lse,
+                                int64_t lse_split_stride, void* out_bf16, int64_t out_row_stride,
+                                float* out_lse, int32_t* dev_status, sps_stream_t stream);
+
+/*
  * sps_dequantize -- exact conversion of quantised inputs to FP16 (the dequant step of "MSA PR
  * 21: Q8KV4 paged sparse prefill", Build the prefill for SM107: an E2M1 code times its E4M3
  * scale is exact in FP16).  The indexer and the forward run it internally on quantised plans.

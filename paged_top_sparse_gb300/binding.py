@@ -85,6 +85,8 @@ def lib(path: str | None = None):
     L.topk_select.argtypes = [vp, vp, i64, vp, vp, vp]
     L.sparse_prefill_fwd.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
     L.partial_combine.argtypes = [i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, vp, vp]
+    L.sparse_prefill_fwd_bf16.argtypes = L.sparse_prefill_fwd.argtypes
+    L.partial_combine_bf16.argtypes = L.partial_combine.argtypes
     L.sparse_prefill_fwd_noalloc.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64,
                                              vp, vp]
     L.sps_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -181,6 +183,16 @@ def sparse_prefill_fwd(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_sca
                                     lse.stride(0), _ptr(workspace), _stream(stream)))
 
 
+def sparse_prefill_fwd_bf16(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
+                            page_table, idx, partial, lse, workspace, stream=None):
+    """As ``sparse_prefill_fwd`` with ``partial`` a BF16 [splits][rows][D] view."""
+    _check(lib().sparse_prefill_fwd_bf16(plan.handle, _ptr(q), float(q_scale), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                         _ptr(page_table), _ptr(idx), _ptr(partial),
+                                         partial.stride(0), _ptr(lse), lse.stride(0),
+                                         _ptr(workspace), _stream(stream)))
+
+
 def sparse_prefill_fwd_noalloc(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
                                page_table, idx, partial, lse, dev_status=None, stream=None):
     """sparse_prefill_fwd without a workspace: the library's own fixed scratch array is used
@@ -197,6 +209,14 @@ def partial_combine(partial, lse, out, out_lse=None, dev_status=None, stream=Non
     _check(lib().partial_combine(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
                                  lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
                                  _ptr(dev_status), _stream(stream)))
+
+
+def partial_combine_bf16(partial, lse, out, out_lse=None, dev_status=None, stream=None):
+    """As ``partial_combine`` with ``partial`` BF16 [splits][rows][D] (rows contiguous)."""
+    S, R, D = partial.shape
+    _check(lib().partial_combine_bf16(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
+                                      lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
+                                      _ptr(dev_status), _stream(stream)))
 
 
 def sps_dequantize(in_dtype: str, data, scales, n: int, out_f16, stream=None):

@@ -5,13 +5,14 @@
 // empty slot (lse = -inf) given weight 0 by selection so its partial is never read.
 //
 // Design (GB300): a persistent grid of 3 CTAs per SM.  A CTA owns tiles of TR consecutive
-// rows (TR * D * 4 bytes = 16 KB, one contiguous chunk of every split slab).  A producer warp
+// rows (TR * D * 4 bytes = 16 KB for FP32 partials, one contiguous chunk of every split slab;
+// BF16 partials, the pages' own storage, take 64 rows per tile).  A producer warp
 // reads the tile's LSEs, computes the weights, and streams each split that has at least one
 // finite LSE in the tile through a 4-slot shared-memory ring with one plain bulk copy
 // (cp.async.bulk) per slot, completion tracked by one mbarrier per slot.  Eight consumer
-// warps accumulate in FP32 registers: each lane owns one float4 column group of 4 rows, so
-// shared-memory reads are conflict-free and the BF16 output of a row is one contiguous
-// 256-byte (D=128) warp store.
+// warps accumulate in FP32 registers: each lane owns one 16-byte column group (4 FP32 or 8
+// BF16 partial values) of a few rows, so shared-memory reads are conflict-free and the BF16
+// output of a row is one contiguous warp store.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -41,18 +42,21 @@ struct __align__(128) CombineSmem {
   int abort_flag;
 };
 
-template <int D>
+// P: partial element type, float or __nv_bfloat16.
+template <int D, typename P>
 __global__ void __launch_bounds__(kThreads, 3)
-combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
+combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
                int64_t split_stride, const float* __restrict__ lse, int64_t lse_split_stride,
                __nv_bfloat16* __restrict__ out, int64_t out_row_stride, float* __restrict__ out_lse,
                int32_t* status) {
-  constexpr int TR = kSlotData / (D * 4);   // rows per tile: 32 (D=128) or 64 (D=64)
-  constexpr int LPR = D / 4;                // lanes per row (one float4 each)
+  constexpr int PE = (int)sizeof(P);
+  constexpr int TR = kSlotData / (D * PE) < 64 ? kSlotData / (D * PE) : 64;  // rows per tile
+  constexpr int EPL = 16 / PE;              // partial values per lane (one 16-byte chunk)
+  constexpr int LPR = D / EPL;              // lanes per row
   constexpr int RPI = 32 / LPR;             // rows per warp instruction
   constexpr int RPW = TR / 8;               // rows per consumer warp
-  constexpr int IT = RPW / RPI;             // float4 items per lane (always 4)
-  static_assert(IT == 4, "layout");
+  constexpr int IT = RPW / RPI;             // 16-byte items per lane
+  static_assert(IT >= 1 && RPW % RPI == 0, "layout");
   extern __shared__ uint8_t smem_raw[];
   CombineSmem& sm = *reinterpret_cast<CombineSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -129,7 +133,7 @@ combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
         if (lane == 0) {
           uint32_t full = smem_u32(&sm.full[slot]);
           if (s >= 0) {
-            uint32_t bytes = (uint32_t)nvalid * D * 4;
+            uint32_t bytes = (uint32_t)nvalid * D * PE;
             mbar_expect_tx(full, bytes);
             bulk_load(smem_u32(sm.data[slot]), partial + s * split_stride + r0 * D, bytes, full);
           } else {
@@ -145,13 +149,17 @@ combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
     // ---------------- consumer warps
     uint32_t slot = 0, phase = 0;
     const int rsub = lane / LPR;        // row within an instruction
-    const int c4 = lane % LPR;          // float4 column group
+    const int c4 = lane % LPR;          // 16-byte column group
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int64_t r0 = tile * TR;
-      float4 acc[IT];
+      float acc[IT][EPL];
       float wsum[IT];
 #pragma unroll
-      for (int i = 0; i < IT; ++i) { acc[i] = make_float4(0.f, 0.f, 0.f, 0.f); wsum[i] = 0.f; }
+      for (int i = 0; i < IT; ++i) {
+        wsum[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[i][e] = 0.f;
+      }
       bool done = false, ok = true;
       while (!done) {
         if (!mbar_wait(smem_u32(&sm.full[slot]), phase, &sm.abort_flag, status)) { ok = false; break; }
@@ -166,12 +174,17 @@ combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
           if (has_data) {
             // a row whose lse is -inf at this split has w == 0 and its partial may hold
             // anything (it was never written): select, never multiply it in
-            const float4 v = reinterpret_cast<const float4*>(sm.data[slot])[rr * LPR + c4];
+            const uint4 raw = reinterpret_cast<const uint4*>(sm.data[slot])[rr * LPR + c4];
+            const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+            float v[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+              if (PE == 4) v[e] = __uint_as_float(wd[e]);
+              else v[e] = __uint_as_float(e & 1 ? wd[e / 2] & 0xffff0000u : wd[e / 2] << 16);
+            }
             const bool use = w != 0.f;
-            acc[i].x = use ? fmaf(w, v.x, acc[i].x) : acc[i].x;
-            acc[i].y = use ? fmaf(w, v.y, acc[i].y) : acc[i].y;
-            acc[i].z = use ? fmaf(w, v.z, acc[i].z) : acc[i].z;
-            acc[i].w = use ? fmaf(w, v.w, acc[i].w) : acc[i].w;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[i][e] = use ? fmaf(w, v[e], acc[i][e]) : acc[i][e];
           }
         }
         float mrow[IT];
@@ -189,12 +202,17 @@ combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
             int64_t r = r0 + rr;
             if (r >= rows) continue;
             float inv = wsum[i] > 0.f ? 1.f / wsum[i] : 0.f;
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&lo);
-            pk.y = *reinterpret_cast<uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(out + r * out_row_stride + c4 * 4) = pk;
+            uint32_t pk[EPL / 2];
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i][e] * inv, acc[i][e + 1] * inv);
+              pk[e / 2] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            if (EPL == 4)
+              *reinterpret_cast<uint2*>(out + r * out_row_stride + c4 * EPL) = make_uint2(pk[0], pk[1]);
+            else
+              *reinterpret_cast<uint4*>(out + r * out_row_stride + c4 * EPL) =
+                  make_uint4(pk[0], pk[1], pk[EPL / 2 > 2 ? 2 : 0], pk[EPL / 2 > 3 ? 3 : 0]);
             if (out_lse && c4 == 0)
               out_lse[r] = wsum[i] > 0.f ? mrow[i] + logf(wsum[i]) : -INFINITY;
           }
@@ -205,30 +223,49 @@ combine_kernel(int64_t rows, int32_t splits, const float* __restrict__ partial,
   }
 }
 
+template <typename P>
+cudaError_t launch_combine_t(int64_t rows, int32_t splits, int32_t D, const P* partial,
+                             int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                             void* out, int64_t out_row_stride, float* out_lse, int32_t* status,
+                             cudaStream_t st) {
+  const int smem = (int)sizeof(CombineSmem) + 128;
+  const int TR = std::min(64, kSlotData / (D * (int)sizeof(P)));
+  int64_t ntiles = (rows + TR - 1) / TR;
+  int64_t grid = std::min<int64_t>(ntiles, 3LL * num_sms());
+  if (grid < 1) return cudaSuccess;
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if (D == 128) {
+    cudaFuncSetAttribute(combine_kernel<128, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    combine_kernel<128, P><<<(unsigned)grid, kThreads, smem, st>>>(
+        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
+        status);
+  } else {
+    cudaFuncSetAttribute(combine_kernel<64, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    combine_kernel<64, P><<<(unsigned)grid, kThreads, smem, st>>>(
+        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
+        status);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_combine(int64_t rows, int32_t splits, int32_t D, const float* partial,
                            int64_t split_stride, const float* lse, int64_t lse_split_stride,
                            void* out, int64_t out_row_stride, float* out_lse, int32_t* status,
                            cudaStream_t st) {
-  const int smem = (int)sizeof(CombineSmem) + 128;
-  const int TR = kSlotData / (D * 4);
-  int64_t ntiles = (rows + TR - 1) / TR;
-  int64_t grid = std::min<int64_t>(ntiles, 3LL * num_sms());
-  if (grid < 1) return cudaSuccess;
-  auto* o = static_cast<__nv_bfloat16*>(out);
-  if (D == 128) {
-    cudaFuncSetAttribute(combine_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    combine_kernel<128><<<(unsigned)grid, kThreads, smem, st>>>(
-        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
-        status);
-  } else {
-    cudaFuncSetAttribute(combine_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    combine_kernel<64><<<(unsigned)grid, kThreads, smem, st>>>(
-        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
-        status);
-  }
-  return cudaGetLastError();
+  return launch_combine_t<float>(rows, splits, D, partial, split_stride, lse, lse_split_stride,
+                                 out, out_row_stride, out_lse, status, st);
+}
+
+cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const void* partial,
+                                 int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                                 void* out, int64_t out_row_stride, float* out_lse,
+                                 int32_t* status, cudaStream_t st) {
+  return launch_combine_t<__nv_bfloat16>(rows, splits, D,
+                                         static_cast<const __nv_bfloat16*>(partial), split_stride,
+                                         lse, lse_split_stride, out, out_row_stride, out_lse,
+                                         status, st);
 }
 
 }  // namespace sps

@@ -39,23 +39,24 @@
 namespace sps {
 namespace {
 
-constexpr int kQS = 2;          // Q ring stages
-
 constexpr int kThreads = 512;   // 4 warpgroups
-template <int D>
-constexpr int stage_pitch() { return D + 4; }  // floats per staging row (pad: conflict-free)
 
-template <int D>
+// PB16: partials are stored as BF16 instead of FP32.  The staging rows then take half the
+// space, which leaves room for a third Q stage.
+template <int D, bool PB16>
 struct FwdSmem {
   static constexpr int TILE = 128 * D * 2;  // 128 rows of D 16-bit elements
+  static constexpr int QS = PB16 ? 3 : 2;   // Q ring stages
+  static constexpr int PE = PB16 ? 2 : 4;   // bytes per partial element
+  static constexpr int SRB = D * PE + 16;   // staging row bytes (pad: conflict-free writes)
   uint8_t k[TILE];
   uint8_t v[TILE];
-  uint8_t q[kQS][TILE];
-  float stage[128 * stage_pitch<D>()];  // one O row per epilogue thread
+  uint8_t q[QS][TILE];
+  alignas(16) uint8_t stage[128 * SRB];  // one O row per epilogue thread
   float inv_l[2][128];
   int2 rs[2][128];
   uint64_t k_full, k_empty, v_full, v_empty, v_ready;
-  uint64_t q_full[kQS], q_empty[kQS];
+  uint64_t q_full[QS], q_empty[QS];
   uint64_t s_full[2], p_full[2], s_free[2], o_full[2], o_empty[2], st_full[2], st_empty[2];
   uint64_t done;
   uint32_t tmem_base;
@@ -63,16 +64,17 @@ struct FwdSmem {
 };
 
 // F16IN: Q, K and V arrive as FP16 (dequantised inputs) instead of BF16; then S = Q K^T runs
-// on FP16 operands and V needs no conversion.
-template <int D, bool F16IN>
+// on FP16 operands and V needs no conversion.  PB16: BF16 partials (see FwdSmem).
+template <int D, bool F16IN, bool PB16>
 __global__ void __launch_bounds__(kThreads, 1)
 forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                DevPlan p,
-               const int32_t* __restrict__ page_table, float* __restrict__ partial,
+               const int32_t* __restrict__ page_table, void* __restrict__ partial,
                int64_t split_stride, float* __restrict__ lse, int64_t lse_split_stride,
                float q_scale) {
-  using Smem = FwdSmem<D>;
+  using Smem = FwdSmem<D, PB16>;
+  constexpr int kQS = Smem::QS;
   constexpr int DB = D / 64;          // 128-byte column blocks of a 16-bit row
   constexpr int TILE = Smem::TILE;
   constexpr int QK_STEPS = D / 16;
@@ -365,14 +367,13 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
     }
   } else if (warp < 12) {
     // ------------------------------------------------ epilogue: warps 8..11
-    // A thread per row: O / l from TMEM into its padded staging row, then one bulk copy of
-    // the whole row (D x 4 bytes) into partial[slot][row].  The stores run on the TMA engine,
-    // so the load/store unit stays free for the producer's Q gather.
-    constexpr int SP = stage_pitch<D>();
+    // A thread per row: O / l from TMEM into its padded staging row (FP32, or BF16 rounded to
+    // nearest even), then one bulk copy of the whole row (D x 4 or D x 2 bytes) into
+    // partial[slot][row].  The stores run on the TMA engine, so the load/store unit stays free.
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    float* srow = sm.stage + row * SP;
+    uint8_t* srow = sm.stage + row * Smem::SRB;
     const uint64_t pol_out = l2_policy_evict_first();  // partials are read once, by the combine
     uint32_t g_it = 0;
     bool ok = true;
@@ -407,18 +408,36 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.o_empty[b]));
           }
+          if (PB16) {
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
+            for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(srow + hh * 64 + cc * 32 + j) = make_float4(
-                  __uint_as_float(v[cc][j]) * inv, __uint_as_float(v[cc][j + 1]) * inv,
-                  __uint_as_float(v[cc][j + 2]) * inv, __uint_as_float(v[cc][j + 3]) * inv);
+              for (int j = 0; j < 32; j += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[cc][j + 2 * u]) * inv,
+                                                            __uint_as_float(v[cc][j + 2 * u + 1]) * inv);
+                  w[u] = *reinterpret_cast<uint32_t*>(&b2);
+                }
+                *reinterpret_cast<uint4*>(srow + (hh * 64 + cc * 32 + j) * 2) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+              }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(srow + (hh * 64 + cc * 32 + j) * 4) = make_float4(
+                    __uint_as_float(v[cc][j]) * inv, __uint_as_float(v[cc][j + 1]) * inv,
+                    __uint_as_float(v[cc][j + 2]) * inv, __uint_as_float(v[cc][j + 3]) * inv);
+          }
         }
         fence_proxy_async_smem();
         if (rs.x >= 0)
-          bulk_store_hint(partial + (int64_t)rs.y * split_stride + (int64_t)rs.x * D,
-                          smem_u32(srow), D * 4, pol_out);
+          bulk_store_hint(static_cast<uint8_t*>(partial) +
+                              ((int64_t)rs.y * split_stride + (int64_t)rs.x * D) * Smem::PE,
+                          smem_u32(srow), D * Smem::PE, pol_out);
         bulk_commit();
       }
     }
@@ -498,9 +517,9 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   }
 }
 
-template <int D, bool F16IN>
+template <int D, bool F16IN, bool PB16>
 cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const void* vc,
-                        const int32_t* page_table, float* partial, int64_t split_stride,
+                        const int32_t* page_table, void* partial, int64_t split_stride,
                         float* lse, int64_t lse_split_stride, float q_scale, cudaStream_t st) {
   alignas(64) CUtensorMap tmQ, tmK, tmV;
   const uint64_t R = (uint64_t)p.T * p.H;
@@ -510,8 +529,8 @@ cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const v
       !encode_tmap_2d(&tmK, dt, const_cast<void*>(kc), D, kv_rows, (uint64_t)D * 2, 64, 128, true) ||
       !encode_tmap_2d(&tmV, dt, const_cast<void*>(vc), D, kv_rows, (uint64_t)D * 2, 64, 128, true))
     return cudaErrorInvalidValue;
-  const int smem = (int)sizeof(FwdSmem<D>) + 1024;
-  auto kern = forward_kernel<D, F16IN>;
+  const int smem = (int)sizeof(FwdSmem<D, PB16>) + 1024;
+  auto kern = forward_kernel<D, F16IN, PB16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreads, smem, st>>>(q, tmQ, tmK, tmV, p, page_table, partial, split_stride,
@@ -519,19 +538,18 @@ cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const v
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
-                           float q_scale, const void* kc, const void* vc, const void* ks,
-                           const void* vs, const int32_t* page_table, float* partial,
-                           int64_t split_stride, float* lse, int64_t lse_split_stride,
-                           cudaStream_t st) {
+template <bool PB16>
+cudaError_t launch_forward_t(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                             float q_scale, const void* kc, const void* vc, const void* ks,
+                             const void* vs, const int32_t* page_table, void* partial,
+                             int64_t split_stride, float* lse, int64_t lse_split_stride,
+                             cudaStream_t st) {
   if (qt == SPS_BF16 && kvt == SPS_BF16) {
     if (p.D == 128)
-      return run_forward<128, false>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                                     lse_split_stride, q_scale, st);
-    return run_forward<64, false>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                                  lse_split_stride, q_scale, st);
+      return run_forward<128, false, PB16>(p, q, kc, vc, page_table, partial, split_stride, lse,
+                                           lse_split_stride, q_scale, st);
+    return run_forward<64, false, PB16>(p, q, kc, vc, page_table, partial, split_stride, lse,
+                                        lse_split_stride, q_scale, st);
   }
   if (qt == SPS_E4M3 && kvt == SPS_NVFP4) {
     // exact FP16 copies of the E4M3 codes and of the NVFP4 products; q_scale stays in the
@@ -543,12 +561,32 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
     if (e == cudaSuccess) e = launch_dequant(SPS_NVFP4, vc, vs, ce, p.vconv, st);
     if (e != cudaSuccess) return e;
     if (p.D == 128)
-      return run_forward<128, true>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
-                                    split_stride, lse, lse_split_stride, q_scale, st);
-    return run_forward<64, true>(p, p.qconv, p.kconv, p.vconv, page_table, partial, split_stride,
-                                 lse, lse_split_stride, q_scale, st);
+      return run_forward<128, true, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
+                                          split_stride, lse, lse_split_stride, q_scale, st);
+    return run_forward<64, true, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
+                                       split_stride, lse, lse_split_stride, q_scale, st);
   }
   return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                           float q_scale, const void* kc, const void* vc, const void* ks,
+                           const void* vs, const int32_t* page_table, float* partial,
+                           int64_t split_stride, float* lse, int64_t lse_split_stride,
+                           cudaStream_t st) {
+  return launch_forward_t<false>(p, qt, kvt, q, q_scale, kc, vc, ks, vs, page_table, partial,
+                                 split_stride, lse, lse_split_stride, st);
+}
+
+cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                                 float q_scale, const void* kc, const void* vc, const void* ks,
+                                 const void* vs, const int32_t* page_table, void* partial,
+                                 int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                 cudaStream_t st) {
+  return launch_forward_t<true>(p, qt, kvt, q, q_scale, kc, vc, ks, vs, page_table, partial,
+                                split_stride, lse, lse_split_stride, st);
 }
 
 }  // namespace sps

@@ -398,12 +398,14 @@ sps_status topk_select(const sps_plan* pl, const float* scores, int64_t score_pi
                   "top-k launch");
 }
 
-sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
-                              const void* k_cache, const void* v_cache, const void* k_scales,
-                              const void* v_scales, const int32_t* page_table,
-                              const int32_t* idx, float* partial, int64_t split_stride,
-                              float* lse, int64_t lse_split_stride, void* ws,
-                              sps_stream_t stream) {
+namespace {
+
+// The forward with FP32 (bf16p = false) or BF16 partials: the same checks and launches.
+sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const void* k_cache,
+                      const void* v_cache, const void* k_scales, const void* v_scales,
+                      const int32_t* page_table, const int32_t* idx, void* partial,
+                      int64_t split_stride, float* lse, int64_t lse_split_stride, void* ws,
+                      sps_stream_t stream, bool bf16p) {
   sps_status st = check_plan_ws(pl, ws);
   if (st != SPS_OK) return st;
   const sps_problem& p = pl->pb;
@@ -415,8 +417,10 @@ sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
       (k_scales && !aligned(k_scales, 16)) || (v_scales && !aligned(v_scales, 16)))
     return fail(SPS_EINVAL, "sparse_prefill_fwd: q/k/v buffers must be 16-byte aligned");
   if (!aligned(partial, 16)) return fail(SPS_EINVAL, "partial must be 16-byte aligned");
-  if (split_stride < pl->R * p.head_dim || split_stride % 4)
-    return fail(SPS_EINVAL, "split_stride must be >= rows*head_dim and a multiple of 4");
+  const int64_t qa = bf16p ? 8 : 4;  // elements per 16 bytes
+  if (split_stride < pl->R * p.head_dim || split_stride % qa)
+    return fail(SPS_EINVAL, "split_stride must be >= rows*head_dim and a multiple of %lld",
+                (long long)qa);
   if (lse_split_stride < pl->R) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
   if (!std::isfinite(q_scale)) return fail(SPS_EINVAL, "q_scale must be finite");
   DevPlan d = make_dev_plan(pl, ws);
@@ -426,16 +430,21 @@ sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
   e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
+  if (bf16p)
+    return launched(launch_forward_bf16p(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
+                                         k_scales, v_scales, page_table, partial, split_stride,
+                                         lse, lse_split_stride, s),
+                    "forward launch");
   return launched(launch_forward(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache, k_scales,
-                                 v_scales, page_table, partial, split_stride, lse,
-                                 lse_split_stride, s),
+                                 v_scales, page_table, static_cast<float*>(partial),
+                                 split_stride, lse, lse_split_stride, s),
                   "forward launch");
 }
 
-sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const float* partial,
-                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
-                           void* out_bf16, int64_t out_row_stride, float* out_lse,
-                           int32_t* dev_status, sps_stream_t stream) {
+sps_status combine_common(int64_t rows, int32_t splits, int32_t head_dim, const void* partial,
+                          int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                          void* out_bf16, int64_t out_row_stride, float* out_lse,
+                          int32_t* dev_status, sps_stream_t stream, bool bf16p) {
   if (rows < 0) return fail(SPS_EINVAL, "rows must be >= 0");
   if (splits < 1 || splits > kMaxTopK) return fail(SPS_EINVAL, "splits must be in [1, 64]");
   if (head_dim != 64 && head_dim != 128) return fail(SPS_EUNSUPPORTED, "head_dim must be 64 or 128");
@@ -443,15 +452,62 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
   if (!partial || !lse || !out_bf16) return fail(SPS_EINVAL, "partial_combine: NULL pointer");
   if (!aligned(partial, 16) || !aligned(out_bf16, 16) || !aligned(lse, 4))
     return fail(SPS_EINVAL, "partial/out must be 16-byte aligned, lse 4-byte aligned");
-  if (split_stride % 4 || split_stride < rows * head_dim)
-    return fail(SPS_EINVAL, "split_stride must be a multiple of 4 and >= rows*head_dim");
+  const int64_t qa = bf16p ? 8 : 4;  // elements per 16 bytes
+  if (split_stride % qa || split_stride < rows * head_dim)
+    return fail(SPS_EINVAL, "split_stride must be a multiple of %lld and >= rows*head_dim",
+                (long long)qa);
   if (lse_split_stride < rows) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
   if (out_row_stride < head_dim || out_row_stride % 8)
     return fail(SPS_EINVAL, "out_row_stride must be >= head_dim and a multiple of 8");
-  return launched(launch_combine(rows, splits, head_dim, partial, split_stride, lse,
-                                 lse_split_stride, out_bf16, out_row_stride, out_lse, dev_status,
-                                 reinterpret_cast<cudaStream_t>(stream)),
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (bf16p)
+    return launched(launch_combine_bf16p(rows, splits, head_dim, partial, split_stride, lse,
+                                         lse_split_stride, out_bf16, out_row_stride, out_lse,
+                                         dev_status, s),
+                    "combine launch");
+  return launched(launch_combine(rows, splits, head_dim, static_cast<const float*>(partial),
+                                 split_stride, lse, lse_split_stride, out_bf16, out_row_stride,
+                                 out_lse, dev_status, s),
                   "combine launch");
+}
+
+}  // namespace
+
+sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
+                              const void* k_cache, const void* v_cache, const void* k_scales,
+                              const void* v_scales, const int32_t* page_table,
+                              const int32_t* idx, float* partial, int64_t split_stride,
+                              float* lse, int64_t lse_split_stride, void* ws,
+                              sps_stream_t stream) {
+  return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
+                    partial, split_stride, lse, lse_split_stride, ws, stream, false);
+}
+
+sps_status sparse_prefill_fwd_bf16(const sps_plan* pl, const void* q, float q_scale,
+                                   const void* k_cache, const void* v_cache,
+                                   const void* k_scales, const void* v_scales,
+                                   const int32_t* page_table, const int32_t* idx,
+                                   void* partial_bf16, int64_t split_stride, float* lse,
+                                   int64_t lse_split_stride, void* ws, sps_stream_t stream) {
+  return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
+                    partial_bf16, split_stride, lse, lse_split_stride, ws, stream, true);
+}
+
+sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const float* partial,
+                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                           void* out_bf16, int64_t out_row_stride, float* out_lse,
+                           int32_t* dev_status, sps_stream_t stream) {
+  return combine_common(rows, splits, head_dim, partial, split_stride, lse, lse_split_stride,
+                        out_bf16, out_row_stride, out_lse, dev_status, stream, false);
+}
+
+sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
+                                const void* partial_bf16, int64_t split_stride, const float* lse,
+                                int64_t lse_split_stride, void* out_bf16, int64_t out_row_stride,
+                                float* out_lse, int32_t* dev_status, sps_stream_t stream) {
+  return combine_common(rows, splits, head_dim, partial_bf16, split_stride, lse,
+                        lse_split_stride, out_bf16, out_row_stride, out_lse, dev_status, stream,
+                        true);
 }
 
 sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales, int64_t n,

@@ -84,6 +84,17 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
                            const void* vs, const int32_t* page_table, float* partial,
                            int64_t split_stride, float* lse, int64_t lse_split_stride,
                            cudaStream_t st);
+// The same forward with BF16 partials (split stride in elements).
+cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                                 float q_scale, const void* kc, const void* vc, const void* ks,
+                                 const void* vs, const int32_t* page_table, void* partial,
+                                 int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                 cudaStream_t st);
+// The combine over BF16 partials.
+cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const void* partial,
+                                 int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                                 void* out, int64_t out_row_stride, float* out_lse,
+                                 int32_t* status, cudaStream_t st);
 
 // One-block kernel whose bounded wait on a never-arrived mbarrier must time out.
 cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t st);

@@ -319,6 +319,89 @@ def test_combine_direct(D, S, R, pad):
     assert np.max(np.abs(gl[fin] - ref_lse[fin])) <= LSE_ATOL
 
 
+@pytest.mark.parametrize("D,S,R,pad", [(128, 16, 1000, 0), (64, 5, 77, 16), (128, 1, 33, 8),
+                                       (128, 64, 129, 0), (64, 16, 300, 0)])
+def test_combine_bf16_direct(D, S, R, pad):
+    """Plan-free combine over BF16 partials: the same cases as the FP32 combine, the oracle
+    merging the identical (exactly widened) BF16 values."""
+    from paged_top_sparse_gb300 import binding as B
+
+    g = torch.Generator().manual_seed(D * 1000 + S * 10 + R + 7)
+    base = torch.randn((S, R * D + pad * 8), generator=g).to(torch.bfloat16)
+    lse = 2.0 * torch.randn((S, R), generator=g)
+    drop = torch.rand((S, R), generator=g) < 0.3
+    lse[drop] = float("-inf")
+    lse[:, R // 2] = float("-inf")
+    pview = base[:, : R * D].view(S, R, D)
+    pview[drop] = float("nan")
+    pv = pview.float().clone()
+    dev = "cuda:0"
+    pd = base.to(dev)
+    partial = pd.as_strided((S, R, D), (R * D + pad * 8, D, 1))
+    ld = lse.to(dev)
+    out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty(R, dtype=torch.float32, device=dev)
+    B.partial_combine_bf16(partial, ld, out, out_lse)
+    torch.cuda.synchronize()
+    ref, ref_lse = orc.combine(np.nan_to_num(pv.numpy(), nan=0.0), lse.numpy())
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert rel_l2(got, ref) <= 2e-3 and np.max(np.abs(got - ref)) <= 1e-2
+    gl = out_lse.cpu().numpy()
+    assert gl[R // 2] == -np.inf and np.all(got[R // 2] == 0)
+    fin = np.isfinite(ref_lse)
+    assert np.max(np.abs(gl[fin] - ref_lse[fin])) <= LSE_ATOL
+
+
+# BF16 partial storage: rounding each partial to BF16 adds a relative error of RMS ~1.6e-3 per
+# element; an FP64 simulation with the oracle (BF16-rounded partials, exact combine, BF16
+# output) moves the output's relative L2 from 1.6e-3 to 1.9e-3 on these shapes, so the bound
+# for this mode is the FP32 path's 2e-3 plus that quadrature term (1.0e-3), rounded up to 3e-3.
+BF16P_OUT_TOL = (3e-3, 1e-2)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "mha_d64", "k1", "quant_small",
+                                  "chunked_fp8_small", "prefill8k"])
+def test_bf16_partials_path(name):
+    """sparse_prefill_fwd_bf16 + partial_combine_bf16 on the FP32 run's selection: each BF16
+    partial is the FP32 path's partial rounded to nearest even (bit-exact), the LSEs are the
+    FP32 path's bit for bit, the combine matches the oracle merge of those BF16 values, and
+    the output matches the direct definition within the bound derived above."""
+    from paged_top_sparse_gb300 import binding as B
+
+    r = _run(name)
+    w, run, rows = r["w"], r["run"], r["rows"]
+    R, K, D = w.num_rows, w.top_k, w.head_dim
+    dev = run.dev
+    pb = torch.full((K, R, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((K, R), float("nan"), dtype=torch.float32, device=dev)
+    B.sparse_prefill_fwd_bf16(run.plan, run.q, run.q_scale, run.k, run.v, run.k_scales,
+                              run.v_scales, run.page_table, run.idx, pb, lse, run.ws)
+    out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    olse = torch.empty((R,), dtype=torch.float32, device=dev)
+    B.partial_combine_bf16(pb, lse, out, olse)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    rows_t = torch.from_numpy(rows).to(dev)
+    live = torch.from_numpy((r["idx"] >= 0).T.copy()).to(dev)  # [K][rows]
+    got_p = pb[:, rows_t]
+    want_p = run.partial[:, rows_t].to(torch.bfloat16)
+    assert torch.equal(got_p[live].view(torch.int16), want_p[live].view(torch.int16))
+    assert torch.equal(lse[:, rows_t], run.lse[:, rows_t])
+    # the combine against the oracle on the same BF16 partials
+    pnp = got_p.float().cpu().numpy().astype(np.float64)
+    lnp = lse[:, rows_t].cpu().numpy().astype(np.float64)
+    ref_c, _ = orc.combine(np.where(np.isfinite(pnp), pnp, 0.0), lnp)
+    got = out[rows_t].float().cpu().numpy()
+    assert rel_l2(got, ref_c) <= 2e-3 and np.max(np.abs(got - ref_c)) <= 1e-2
+    # end to end against the direct definition
+    q, k, v, qi, ki = oracle_tensors(w, r["t"])
+    ref, _ = orc.dense(oracle_problem(w), q, k, v, w.sm_scale, r["idx"], rows)
+    tol = BF16P_OUT_TOL if w.kv_dtype == "bf16" else (OUT_TOL["quant"][0] + 1e-3,
+                                                      OUT_TOL["quant"][1])
+    assert rel_l2(got, ref) <= tol[0] and np.max(np.abs(got - ref)) <= tol[1]
+
+
 def test_bad_page_table_entry_sets_status():
     """An out-of-range physical page is caught on the device: status, no fault."""
     from tests.gpu_helpers import DeviceRun
