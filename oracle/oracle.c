@@ -28,6 +28,9 @@
  *   decode           BF16 / FP16 / E4M3 / NVFP4 (E2M1 code x E4M3 per-16 scale) bit-field
  *                    decode from the format definitions ("MSA PR 21", Build the prefill for
  *                    SM107: the code-times-scale product).
+ *   quantise, append the chunked-prefill step before the indexer: E4M3 / E2M1 rounding
+ *                    (nearest, ties to even, saturating), NVFP4 blocks (scale E4M3(absmax/6)),
+ *                    and the paged write of new tokens' K/V through the page table.
  *
  * Every sum is accumulated in double.  Functions take an optional row subset so that the
  * full-size workloads can be checked on sampled rows.
@@ -393,6 +396,105 @@ void orc_dense(const orc_problem* pb, orc_tensor q, orc_tensor k, orc_tensor v, 
     free(logit);
     free(kphys);
     free(kj);
+  }
+}
+
+/* ---------------------------------------------------------------- quantisation */
+/*
+ * The step before the indexer in chunked prefill: the new tokens' K/V enter the paged cache,
+ * quantised where the cache is quantised, and the query is quantised to E4M3 with a
+ * per-tensor scale.  The formats are the ones decoded above; the pages fix no rounding for
+ * this step, so the plainest one is used: every division in binary32, every conversion
+ * round-to-nearest with ties to the even code, saturating at the largest finite value.
+ */
+
+/* Nearest value on a grid with `mbits` mantissa bits, exponent bias `bias` and largest code
+ * `maxcode` (magnitude bits); returns the magnitude code.  a >= 0, finite. */
+static uint32_t round_minifloat(double a, int mbits, int bias, uint32_t maxcode, double maxval) {
+  if (a >= maxval) return maxcode;
+  const double sub_ulp = ldexp(1.0, 1 - bias - mbits);  /* spacing below the first normal */
+  const double min_normal = ldexp(1.0, 1 - bias);
+  if (a < min_normal) {
+    /* n in [0, 2^mbits]; 2^mbits is the first normal, whose code is the same integer */
+    return (uint32_t)rint(a / sub_ulp);
+  }
+  int e = ilogb(a);                       /* a in [2^e, 2^(e+1)) */
+  double ulp = ldexp(1.0, e - mbits);
+  double n = rint(a / ulp);               /* in [2^mbits, 2^(mbits+1)] */
+  if (n >= ldexp(1.0, mbits + 1)) { e += 1; n = ldexp(1.0, mbits); }
+  uint32_t code = ((uint32_t)(e + bias) << mbits) | (uint32_t)(n - ldexp(1.0, mbits));
+  return code > maxcode ? maxcode : code;
+}
+
+/* binary32 -> OCP E4M3 (largest finite 448, code 0x7E), ties to even, saturating. */
+uint8_t orc_round_e4m3(float x) {
+  const uint32_t mag = round_minifloat(fabs((double)x), 3, 7, 0x7E, 448.0);
+  return (uint8_t)((signbit(x) ? 0x80u : 0u) | mag);
+}
+
+/* binary32 -> OCP E2M1 nibble (largest 6, code 7), ties to even, saturating. */
+uint8_t orc_round_e2m1(float x) {
+  const uint32_t mag = round_minifloat(fabs((double)x), 1, 1, 0x7, 6.0);
+  return (uint8_t)((signbit(x) ? 0x8u : 0u) | mag);
+}
+
+/* Element-wise versions for arrays. */
+void orc_round_e4m3_n(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_round_e4m3(x[i]);
+}
+void orc_round_e2m1_n(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_round_e2m1(x[i]);
+}
+
+/* One NVFP4 block of 16 BF16 values: scale = E4M3(absmax / 6), code_i = E2M1(x_i / scale),
+ * both divisions in binary32; a block whose scale rounds to zero gets zero codes.  codes[]
+ * receives 8 bytes, element 2i in the low nibble of byte i. */
+void orc_quantize_nvfp4_block(const uint16_t* x_bf16, uint8_t* codes, uint8_t* scale) {
+  float x[16], amax = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    x[i] = (float)orc_decode_bf16(x_bf16[i]);
+    const float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  const float s32 = amax / 6.0f;
+  *scale = orc_round_e4m3(s32);
+  const float sv = (float)orc_decode_e4m3(*scale);
+  for (int i = 0; i < 16; i += 2) {
+    const uint8_t lo = sv == 0.0f ? 0 : orc_round_e2m1(x[i] / sv);
+    const uint8_t hi = sv == 0.0f ? 0 : orc_round_e2m1(x[i + 1] / sv);
+    codes[i / 2] = (uint8_t)(lo | (hi << 4));
+  }
+}
+
+/* E4M3 codes of n BF16 values with a per-tensor scale: code = E4M3(x / scale). */
+void orc_quantize_e4m3(const uint16_t* x_bf16, int64_t n, float scale, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = orc_round_e4m3((float)orc_decode_bf16(x_bf16[i]) / scale);
+}
+
+/* Paged append: token i of request b (flat token index tk, position t = ctx_len[b] + i) goes
+ * to physical page page_table[b][t / P], slot t % P, for every kv head.  new_bf16 is
+ * [T][H_kv][D].  kv_dtype ORC_BF16: cache_bf16 [phys][H_kv][P][D] receives the bits;
+ * ORC_NVFP4: codes [phys][H_kv][P][D/2] and scales [phys][H_kv][P][D/16]. */
+void orc_kv_append(const orc_problem* pb, int32_t kv_dtype, const uint16_t* new_bf16,
+                   void* cache, uint8_t* scales) {
+  const int D = pb->head_dim, G = pb->num_kv_heads, P = pb->page_size;
+  int64_t tk = 0;
+  for (int b = 0; b < pb->batch; ++b) {
+    for (int i = 0; i < pb->q_lens[b]; ++i, ++tk) {
+      const int32_t t = pb->ctx_lens[b] + i;
+      const int32_t phys = pb->page_table[(int64_t)b * pb->max_pages + t / P];
+      for (int g = 0; g < G; ++g) {
+        const uint16_t* src = new_bf16 + (tk * G + g) * D;
+        const int64_t slot = ((int64_t)phys * G + g) * P + t % P;
+        if (kv_dtype == ORC_BF16) {
+          memcpy((uint16_t*)cache + slot * D, src, sizeof(uint16_t) * D);
+        } else {
+          for (int blk = 0; blk < D / 16; ++blk)
+            orc_quantize_nvfp4_block(src + blk * 16, (uint8_t*)cache + slot * (D / 2) + blk * 8,
+                                     scales + slot * (D / 16) + blk);
+        }
+      }
+    }
   }
 }
 

@@ -87,6 +87,11 @@ def lib():
         _lib.orc_combine.argtypes = [i64, i32, i32, vp, i64, i64, vp, i64, vp, vp]
         _lib.orc_dense.argtypes = [P, T, T, T, dbl, vp, vp, i64, vp, vp]
         _lib.orc_num_threads.restype = ctypes.c_int
+        _lib.orc_round_e4m3_n.argtypes = [vp, i64, vp]
+        _lib.orc_round_e2m1_n.argtypes = [vp, i64, vp]
+        _lib.orc_quantize_nvfp4_block.argtypes = [vp, vp, vp]
+        _lib.orc_quantize_e4m3.argtypes = [vp, i64, ctypes.c_float, vp]
+        _lib.orc_kv_append.argtypes = [P, i32, vp, vp, vp]
     return _lib
 
 
@@ -161,6 +166,55 @@ def _rows(pb: Problem, rows):
     if rows is None:
         rows = np.arange(pb.num_rows, dtype=np.int64)
     return np.ascontiguousarray(rows, dtype=np.int64)
+
+
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """binary32 -> E4M3 codes: nearest, ties to the even code, saturating at +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().orc_round_e4m3_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def round_e2m1(x: np.ndarray) -> np.ndarray:
+    """binary32 -> E2M1 nibbles: nearest, ties to the even code, saturating at +-6."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().orc_round_e2m1_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_nvfp4(x_bf16: np.ndarray):
+    """BF16 bits [..., 16 m] -> (codes [..., 8 m] uint8, scales [..., m] uint8), block by
+    block: scale = E4M3(absmax / 6), code = E2M1(x / scale)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    n = x.size // 16
+    codes = np.empty(n * 8, np.uint8)
+    scales = np.empty(n, np.uint8)
+    flat = x.reshape(-1)
+    L = lib()
+    for b in range(n):
+        blk = flat[16 * b: 16 * b + 16]
+        L.orc_quantize_nvfp4_block(_ptr(blk), _ptr(codes[8 * b:]), _ptr(scales[b:]))
+    return codes.reshape(x.shape[:-1] + (x.shape[-1] // 2,)), scales.reshape(x.shape[:-1] + (x.shape[-1] // 16,))
+
+
+def quantize_e4m3(x_bf16: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes of BF16 values with a per-tensor scale: E4M3(x / scale) in binary32."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    lib().orc_quantize_e4m3(_ptr(x), x.size, ctypes.c_float(scale), _ptr(out))
+    return out
+
+
+def kv_append(pb: Problem, kv_dtype: str, new_bf16: np.ndarray, cache: np.ndarray,
+              scales: np.ndarray | None = None):
+    """Writes the batch's new tokens ``new_bf16`` [T][H_kv][D] (BF16 bits) into ``cache`` in
+    place: BF16 bits [phys][H_kv][P][D], or NVFP4 codes [phys][H_kv][P][D/2] with ``scales``
+    [phys][H_kv][P][D/16]."""
+    x = np.ascontiguousarray(new_bf16, dtype=np.uint16)
+    assert cache.flags.c_contiguous and (scales is None or scales.flags.c_contiguous)
+    lib().orc_kv_append(ctypes.byref(pb.c()), DTYPES[kv_dtype], _ptr(x), _ptr(cache), _ptr(scales))
 
 
 def num_threads() -> int:

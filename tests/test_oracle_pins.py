@@ -358,3 +358,126 @@ def test_inversion_matches_dict_buckets():
     for bk in range(nb):
         lst = list(zip(er[offsets[bk]:offsets[bk + 1]], es[offsets[bk]:offsets[bk + 1]]))
         assert lst == sorted(buckets.get(bk, [])), bk
+
+
+# ---------------------------------------------------------------- quantisation / append
+
+def _e4m3_ties_and_edges(rng):
+    """Random finite values plus every exact midpoint between neighbouring E4M3 values, the
+    subnormal range and values just beside the midpoints."""
+    codes = np.arange(0, 0x7F, dtype=np.uint8)
+    dec = np.array([orc.lib().orc_decode_e4m3(int(c)) for c in codes])
+    mids = (dec[:-1] + dec[1:]) / 2.0
+    near = np.concatenate([mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                           np.nextafter(mids.astype(np.float32), np.float32(1e9))])
+    rnd = rng.standard_normal(20000) * np.exp(rng.uniform(-9, 6, 20000))
+    allv = np.concatenate([dec, near, rnd])
+    allv = allv[np.abs(allv) <= 448]
+    return np.concatenate([allv, -allv]).astype(np.float32)
+
+
+def test_e4m3_rounding_matches_torch_ties_to_even():
+    """orc.round_e4m3 against torch's float8_e4m3fn conversion (round to nearest even) on every
+    midpoint, the subnormals and random values; beyond 448 it saturates to the 0x7E code."""
+    rng = np.random.default_rng(41)
+    x = _e4m3_ties_and_edges(rng)
+    got = orc.round_e4m3(x)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # -0.0 and +0.0 may differ only in the sign bit for inputs that are zero
+    assert np.array_equal(got, want)
+    big = np.array([448.0, 449.0, 464.0, 480.0, 1e6, -500.0], np.float32)
+    assert list(orc.round_e4m3(big)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_e2m1_rounding_matches_bruteforce_nearest():
+    """orc.round_e2m1 against a direct search over the eight magnitudes (nearest value, ties
+    to the even code, saturating at 6) on a dense grid including every midpoint."""
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    grid = np.concatenate([np.arange(0, 8.0, 1 / 64), (mags[:-1] + mags[1:]) / 2, [6.0, 7.0, 1e3]])
+    x = np.concatenate([grid, -grid]).astype(np.float32)
+    want = []
+    for v in x.astype(np.float64):
+        a = abs(v)
+        d = np.abs(mags - a)
+        best = np.flatnonzero(d == d.min())
+        code = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+        want.append(code | (8 if np.signbit(v) else 0))
+    assert np.array_equal(orc.round_e2m1(x), np.array(want, np.uint8))
+
+
+def test_nvfp4_block_quantisation_worked_example():
+    """A block whose absmax is 6 has scale 1 (E4M3 0x38) and its codes are the E2M1 roundings
+    of the values themselves; doubling every value doubles the scale and keeps the codes; a
+    zero block gets scale 0 and zero codes."""
+    vals = np.array([6, -6, 0.25, 0.75, 1.25, 2.5, 5, -3, 0.5, 1, 1.5, 2, 3, 4, -0.5, 0],
+                    np.float32)
+    bits = synth.f32_to_bf16_bits(vals)
+    codes, scales = orc.quantize_nvfp4(bits[None, :])
+    assert scales[0, 0] == 0x38
+    nib = np.stack([codes[0] & 0xF, codes[0] >> 4], 1).reshape(-1)
+    assert np.array_equal(nib, orc.round_e2m1(vals))
+    codes2, scales2 = orc.quantize_nvfp4(synth.f32_to_bf16_bits(vals * 2)[None, :])
+    assert orc.lib().orc_decode_e4m3(int(scales2[0, 0])) == 2.0 and np.array_equal(codes2, codes)
+    codes0, scales0 = orc.quantize_nvfp4(synth.f32_to_bf16_bits(np.zeros(16, np.float32))[None, :])
+    assert scales0[0, 0] == 0 and not codes0.any()
+
+
+def test_nvfp4_quantisation_error_bound_and_decode_roundtrip():
+    """On random blocks: the scale is E4M3(absmax/6); every decoded element is within half an
+    E2M1 step of x (at the block's scale), or clipped at 6 x scale; decoding then
+    re-quantising reproduces the codes when the block keeps its scale."""
+    rng = np.random.default_rng(43)
+    x = (rng.standard_normal((300, 16)) * np.exp(rng.uniform(-6, 6, (300, 1)))).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    codes, scales = orc.quantize_nvfp4(bits)
+    amax = np.abs(xb).max(1)
+    assert np.array_equal(scales[:, 0], orc.round_e4m3((amax / np.float32(6)).astype(np.float32)))
+    t = orc.Tensor(codes, "nvfp4", scales=scales)
+    dec = orc.decode(t).reshape(300, 16)
+    sv = np.array([orc.lib().orc_decode_e4m3(int(s)) for s in scales[:, 0]])
+    # E2M1 spacing at |x|/s: 0.5 below 2, 1 up to 4, 2 up to 6
+    with np.errstate(divide="ignore"):  # a block whose scale rounds to 0 has zero codes
+        q = np.abs(xb) / sv[:, None]
+    half_step = np.where(q < 2, 0.25, np.where(q < 4, 0.5, 1.0)) * sv[:, None]
+    clipped = q > 6
+    assert np.all((np.abs(dec - xb) <= half_step + 1e-12) | clipped)
+    assert np.all(np.abs(dec[clipped]) == 6 * np.repeat(sv[:, None], 16, 1)[clipped])
+
+
+def test_kv_append_places_tokens_through_page_table():
+    """BF16 append: decoding the cache at (page_table[b][t/P], g, t%P) gives back every new
+    token's row; every other slot keeps its previous bits.  NVFP4 append: the slot holds the
+    block quantisation of the row and nothing else changes."""
+    w = synth.workload("custom", seed=44, q_lens=[130, 5, 256], ctx_lens=[100, 383, 0],
+                       num_q_heads=4, num_kv_heads=2, head_dim=64, top_k=2)
+    pb = oracle_problem(w)
+    rng = np.random.default_rng(45)
+    T, G, D, P = w.num_tokens, w.num_kv_heads, w.head_dim, 128
+    new = synth.f32_to_bf16_bits(rng.standard_normal((T, G, D)).astype(np.float32))
+    cache = synth.f32_to_bf16_bits(rng.standard_normal((w.num_phys_pages, G, P, D)).astype(np.float32))
+    before = cache.copy()
+    orc.kv_append(pb, "bf16", new, cache)
+    written = np.zeros((w.num_phys_pages, G, P), bool)
+    tk = 0
+    for b, (ql, cl) in enumerate(zip(w.q_lens, w.ctx_lens)):
+        for i in range(ql):
+            t = cl + i
+            phys = w.page_table[b, t // P]
+            assert np.array_equal(cache[phys, :, t % P], new[tk])
+            written[phys, :, t % P] = True
+            tk += 1
+    assert np.array_equal(cache[~written], before[~written])
+    codes = np.zeros((w.num_phys_pages, G, P, D // 2), np.uint8)
+    scl = np.zeros((w.num_phys_pages, G, P, D // 16), np.uint8)
+    orc.kv_append(pb, "nvfp4", new, codes, scl)
+    qc, qs = orc.quantize_nvfp4(new)
+    tk = 0
+    for b, (ql, cl) in enumerate(zip(w.q_lens, w.ctx_lens)):
+        for i in range(ql):
+            t = cl + i
+            phys = w.page_table[b, t // P]
+            assert np.array_equal(codes[phys, :, t % P], qc[tk])
+            assert np.array_equal(scl[phys, :, t % P], qs[tk])
+            tk += 1
+    assert not codes[~written].any() and not scl[~written].any()
