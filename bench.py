@@ -144,7 +144,7 @@ def _algorithmic(w, idx_np, partial_bytes=4):
     }
 
 
-WORKLOADS = ("prefill8k", "prefill8k_q", "chunked32k", "combine_stress")
+WORKLOADS = ("prefill8k", "prefill8k_q", "chunked32k", "combine_stress", "kv_append")
 
 
 def _workload(args):
@@ -253,6 +253,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     if args.workload == "combine_stress":
         return run_combine_stress(args, rank, world, dev)
+    if args.workload == "kv_append":
+        return run_kv_append(args, rank, world, dev)
     from paged_top_sparse_gb300 import synth
 
     w = _workload(args)
@@ -453,6 +455,79 @@ def run_combine_stress(args, rank, world, dev):
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": hp.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": hout.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(t_wall, 3),
+    }
+    return line, None, None
+
+
+def run_kv_append(args, rank, world, dev):
+    """The chunked-prefill append alone: 8 requests x 512 new tokens (2 KV heads, D 128) into
+    an NVFP4 paged cache over ~32K of context; tokens/s = new tokens / append time."""
+    import torch
+
+    from paged_top_sparse_gb300 import binding as B
+    from paged_top_sparse_gb300 import synth
+
+    base = synth.workload("chunked32k", seed=args.seed)
+    w = synth.workload("custom", seed=args.seed, q_lens=list(base.q_lens),
+                       ctx_lens=list(base.ctx_lens), num_q_heads=32, num_kv_heads=2,
+                       head_dim=128, top_k=16, q_dtype="e4m3", kv_dtype="nvfp4")
+    T, G, D, NP = w.num_tokens, w.num_kv_heads, w.head_dim, w.num_phys_pages
+    rng = np.random.default_rng(args.seed)
+    knew = synth.f32_to_bf16_bits(rng.standard_normal((T, G, D)).astype(np.float32))
+    vnew = synth.f32_to_bf16_bits(rng.standard_normal((T, G, D)).astype(np.float32))
+    hk, hv = _pinned(knew), _pinned(vnew)
+    dk, dv = hk.to(dev), hv.to(dev)
+    kc = torch.zeros((NP, G, 128, D // 2), dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((NP, G, 128, D // 16), dtype=torch.uint8, device=dev)
+    vs = torch.zeros_like(ks)
+    pt = torch.from_numpy(w.page_table.astype(np.int32)).to(dev)
+    plan = B.Plan(w.q_lens, w.ctx_lens, w.num_q_heads, G, D, w.top_k, w.max_pages, NP,
+                  q_dtype="e4m3", kv_dtype="nvfp4")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    B.sps_plan_upload(plan, ws)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(ev, k_=dk, v_=dv):
+        if ev: ev[0].record(torch.cuda.current_stream())
+        B.sps_kv_append(plan, k_, v_, pt, kc, vc, ks, vs, ws)
+        if ev: ev[1].record(torch.cuda.current_stream())
+
+    per, clocks, t_wall, stream = _timed_loop(args, world, dev, flush, step, 1)
+    assert B.sps_read_device_status(plan, ws) == 0
+    ms = float(per[:, 0].mean())
+    ek, ev_ = torch.empty_like(dk), torch.empty_like(dv)
+
+    def copy_in():
+        ek.copy_(hk, non_blocking=True)
+        ev_.copy_(hv, non_blocking=True)
+
+    e2e_ms = _e2e(args, flush, stream, copy_in, lambda e: step(e, ek, ev_), lambda: None)
+    clk = clocks.stop()
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world)
+    hbm, _, peak_kind = _peaks()
+    alg = T * G * D * 2 * 2 + T * G * (D // 2 + D // 16) * 2  # read BF16 K/V, write codes + scales
+    ach = alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(job_tokens_per_s(T, world, ms), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) BF16 K/V)",
+        "config": {"workload": f"kv append: {w.batch} requests x 512 new tokens into an NVFP4 "
+                               f"paged cache over {min(w.ctx_lens)}..{max(w.ctx_lens)} cached, "
+                               "2 KV heads, head_dim 128", "tokens": int(T),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MB flush between steps"},
+        "roofline": {"bound": "hbm", "kernel": "kv_append", "achieved": round(ach, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"
+                     if peak_kind == "measured" else "fallback", "traffic": None},
+        "e2e": {"value": round(job_tokens_per_s(T, world, e2e_ms), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": hk.numel() * 2 * 2,
+                "d2h_bytes_per_step": 0},
         "gpu_launches": args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),

@@ -252,6 +252,37 @@ sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
                                 float* out_lse, int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sps_kv_append -- the chunked-prefill step before indexer_scores: writes the batch's new
+ * tokens' K and V into the paged cache (the formats of "MSA PR 21: Q8KV4 paged sparse
+ * prefill": E4M3 query, NVFP4 K/V with an E4M3 scale per 16 elements; the pages fix no
+ * rounding for this step).  Token i of request b (position t = ctx_len + i, flat token order
+ * of the plan) goes to physical page page_table[b][t / 128], slot t % 128, of every KV head.
+ *   k_new, v_new  device BF16 [T][H_kv][D], 16-byte aligned
+ *   k_cache, v_cache  the plan's kv_dtype: BF16 [num_phys_pages][H_kv][128][D] (bits copied),
+ *                 or NVFP4 codes [..][128][D/2] with k_scales / v_scales [..][128][D/16]:
+ *                 per 16-element block scale = E4M3(absmax / 6), code = E2M1(x / scale), both
+ *                 divisions in FP32, conversions to nearest even and saturating; a block whose
+ *                 scale rounds to zero gets zero codes
+ *   workspace     the plan's uploaded workspace (token positions); a page-table entry outside
+ *                 [0, num_phys_pages) sets SPS_DEV_BAD_PAGE and skips the row
+ * Slots not written keep their contents.
+ */
+sps_status sps_kv_append(const sps_plan* plan, const void* k_new, const void* v_new,
+                         const int32_t* page_table, void* k_cache, void* v_cache, void* k_scales,
+                         void* v_scales, void* workspace, sps_stream_t stream);
+
+/*
+ * sps_quantize_e4m3 -- per-tensor E4M3 query codes: codes[i] = E4M3(x[i] / scale) (FP32
+ * division, nearest even, saturating at 448); x BF16, n a multiple of 16, both 16-byte
+ * aligned, scale finite and > 0 (the pages' E4M3 query with its per-tensor scale).
+ * sps_absmax_bf16 -- *absmax (device FP32) = max |x[i]| over n BF16 values (n a multiple of
+ * 16), e.g. for scale = absmax / 448.
+ */
+sps_status sps_quantize_e4m3(const void* x_bf16, int64_t n, float scale, void* codes,
+                             sps_stream_t stream);
+sps_status sps_absmax_bf16(const void* x_bf16, int64_t n, float* absmax, sps_stream_t stream);
+
+/*
  * sps_dequantize -- exact conversion of quantised inputs to FP16 (the dequant step of "MSA PR
  * 21: Q8KV4 paged sparse prefill", Build the prefill for SM107: an E2M1 code times its E4M3
  * scale is exact in FP16).  The indexer and the forward run it internally on quantised plans.

@@ -86,6 +86,9 @@ def lib(path: str | None = None):
     L.sparse_prefill_fwd.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
     L.partial_combine.argtypes = [i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, vp, vp]
     L.sparse_prefill_fwd_bf16.argtypes = L.sparse_prefill_fwd.argtypes
+    L.sps_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.sps_quantize_e4m3.argtypes = [vp, i64, f32, vp, vp]
+    L.sps_absmax_bf16.argtypes = [vp, i64, vp, vp]
     L.partial_combine_bf16.argtypes = L.partial_combine.argtypes
     L.sparse_prefill_fwd_noalloc.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64,
                                              vp, vp]
@@ -217,6 +220,25 @@ def partial_combine_bf16(partial, lse, out, out_lse=None, dev_status=None, strea
     _check(lib().partial_combine_bf16(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
                                       lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
                                       _ptr(dev_status), _stream(stream)))
+
+
+def sps_kv_append(plan: Plan, k_new, v_new, page_table, k_cache, v_cache, k_scales, v_scales,
+                  workspace, stream=None):
+    """New tokens' K/V [T][H_kv][D] BF16 into the paged cache (the plan's kv dtype)."""
+    _check(lib().sps_kv_append(plan.handle, _ptr(k_new), _ptr(v_new), _ptr(page_table),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                               _ptr(workspace), _stream(stream)))
+
+
+def sps_quantize_e4m3(x_bf16, scale: float, codes, stream=None):
+    """E4M3 codes of ``x_bf16`` (any shape, n % 16 == 0) with a per-tensor scale."""
+    _check(lib().sps_quantize_e4m3(_ptr(x_bf16), x_bf16.numel(), float(scale), _ptr(codes),
+                                   _stream(stream)))
+
+
+def sps_absmax_bf16(x_bf16, out_f32, stream=None):
+    """out_f32[0] = max |x| over ``x_bf16`` (device)."""
+    _check(lib().sps_absmax_bf16(_ptr(x_bf16), x_bf16.numel(), _ptr(out_f32), _stream(stream)))
 
 
 def sps_dequantize(in_dtype: str, data, scales, n: int, out_f16, stream=None):

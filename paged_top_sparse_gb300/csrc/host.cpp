@@ -510,6 +510,50 @@ sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
                         true);
 }
 
+sps_status sps_kv_append(const sps_plan* pl, const void* k_new, const void* v_new,
+                         const int32_t* page_table, void* k_cache, void* v_cache, void* k_scales,
+                         void* v_scales, void* ws, sps_stream_t stream) {
+  sps_status st = check_plan_ws(pl, ws);
+  if (st != SPS_OK) return st;
+  const sps_problem& p = pl->pb;
+  const bool nvfp4 = p.kv_dtype == SPS_NVFP4;
+  if (p.kv_dtype != SPS_BF16 && !nvfp4)
+    return fail(SPS_EUNSUPPORTED, "sps_kv_append: the cache must be BF16 or NVFP4");
+  if (!k_new || !v_new || !page_table || !k_cache || !v_cache)
+    return fail(SPS_EINVAL, "sps_kv_append: NULL pointer");
+  if (nvfp4 && (!k_scales || !v_scales))
+    return fail(SPS_EINVAL, "sps_kv_append: an NVFP4 cache needs k_scales and v_scales");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(page_table, 4))
+    return fail(SPS_EINVAL, "sps_kv_append: buffers must be 16-byte aligned");
+  DevPlan d = make_dev_plan(pl, ws);
+  return launched(launch_kv_append(d, nvfp4, k_new, v_new, page_table, k_cache, v_cache, k_scales,
+                                   v_scales, reinterpret_cast<cudaStream_t>(stream)),
+                  "kv append launch");
+}
+
+sps_status sps_quantize_e4m3(const void* x_bf16, int64_t n, float scale, void* codes,
+                             sps_stream_t stream) {
+  if (n < 0 || n % 16) return fail(SPS_EINVAL, "sps_quantize_e4m3: n must be a multiple of 16");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(SPS_EINVAL, "sps_quantize_e4m3: scale must be finite and > 0");
+  if (n == 0) return SPS_OK;
+  if (!x_bf16 || !codes || !aligned(x_bf16, 16) || !aligned(codes, 16))
+    return fail(SPS_EINVAL, "sps_quantize_e4m3: buffers must be non-NULL and 16-byte aligned");
+  return launched(launch_quantize_e4m3(x_bf16, n, scale, codes,
+                                       reinterpret_cast<cudaStream_t>(stream)),
+                  "quantize launch");
+}
+
+sps_status sps_absmax_bf16(const void* x_bf16, int64_t n, float* absmax, sps_stream_t stream) {
+  if (n < 0 || n % 16) return fail(SPS_EINVAL, "sps_absmax_bf16: n must be a multiple of 16");
+  if (!absmax || !aligned(absmax, 4)) return fail(SPS_EINVAL, "sps_absmax_bf16: bad output");
+  if (n > 0 && (!x_bf16 || !aligned(x_bf16, 16)))
+    return fail(SPS_EINVAL, "sps_absmax_bf16: input must be non-NULL and 16-byte aligned");
+  return launched(launch_absmax_bf16(x_bf16, n, absmax, reinterpret_cast<cudaStream_t>(stream)),
+                  "absmax launch");
+}
+
 sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales, int64_t n,
                           void* out_f16, sps_stream_t stream) {
   if (in_dtype != SPS_E4M3 && in_dtype != SPS_NVFP4)

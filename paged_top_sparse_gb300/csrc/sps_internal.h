@@ -96,6 +96,15 @@ cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const 
                                  void* out, int64_t out_row_stride, float* out_lse,
                                  int32_t* status, cudaStream_t st);
 
+// Chunked-prefill append of the new tokens' K/V into the paged cache (BF16 copy or NVFP4
+// quantisation), per-tensor E4M3 quantisation, and the BF16 absmax behind its scale.
+cudaError_t launch_kv_append(const DevPlan& p, bool nvfp4, const void* knew, const void* vnew,
+                             const int32_t* page_table, void* kc, void* vc, void* ks, void* vs,
+                             cudaStream_t st);
+cudaError_t launch_quantize_e4m3(const void* in, int64_t n, float scale, void* out,
+                                 cudaStream_t st);
+cudaError_t launch_absmax_bf16(const void* in, int64_t n, float* out, cudaStream_t st);
+
 // One-block kernel whose bounded wait on a never-arrived mbarrier must time out.
 cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t st);
 
