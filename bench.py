@@ -281,6 +281,10 @@ def run_gpu(args, rank, world):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     fwd_call = B.sparse_prefill_fwd_bf16 if bf16p else B.sparse_prefill_fwd
+    if args.fp8qk:
+        if bf16p or w.kv_dtype != "nvfp4":
+            raise SystemExit("--fp8qk needs the quantised workload (prefill8k_q) and FP32 partials")
+        fwd_call = B.sparse_prefill_fwd_fp8qk
     combine_call = B.partial_combine_bf16 if bf16p else B.partial_combine
 
     def step(ev, di=din):
@@ -366,7 +370,8 @@ def run_gpu(args, rank, world):
         "dtype": "fp16" if w.kv_dtype == "nvfp4" else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, quantised where the workload says; permuted "
                 "page table)",
-        "config": {"workload": _describe(w, args.workload) + (", BF16 partials" if bf16p else ""),
+        "config": {"workload": _describe(w, args.workload) + (", BF16 partials" if bf16p else "")
+                               + (", FP8 Q K^T on E4M3-rounded K" if args.fp8qk else ""),
                    "partials": "bf16" if bf16p else "fp32",
                    "batch": int(w.batch), "seq_len": int(max(w.q_lens)), "rows": int(R),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -606,6 +611,9 @@ def main():
     ap.add_argument("--workload", default="prefill8k", choices=WORKLOADS,
                     help="prefill8k (default: the headline line), prefill8k_q (E4M3 Q, NVFP4 "
                          "K/V), chunked32k (8 x 512 over 32K context), combine_stress")
+    ap.add_argument("--fp8qk", action="store_true",
+                    help="quantised workload only: the pages' Q8KV4 route (K rounded to E4M3, "
+                         "FP8 Q K^T) through sparse_prefill_fwd_fp8qk")
     ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
                     help="partial storage: fp32 (the contract; default) or bf16 (the pages' "
                          "storage, sparse_prefill_fwd_bf16 + partial_combine_bf16)")

@@ -252,6 +252,22 @@ sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
                                 float* out_lse, int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sparse_prefill_fwd_fp8qk -- the pages' own Q8KV4 route ("MSA PR 21: Q8KV4 paged sparse
+ * prefill": QMUL4 dequant, whose only rounding is the final conversion of the code x scale
+ * product to E4M3, and FP8 UMMA for Q K^T): the same arguments and outputs as
+ * sparse_prefill_fwd for a plan with E4M3 Q, NVFP4 K/V and head_dim 128.  K is rounded to
+ * E4M3 (nearest even, saturating), S = Q K^T runs on the FP8 tensor core (FP32 accumulation);
+ * V stays exact (FP16) for P.V.  Its results match the definition on the E4M3-rounded K, not
+ * on the exact products; other plans return SPS_EUNSUPPORTED.
+ */
+sps_status sparse_prefill_fwd_fp8qk(const sps_plan* plan, const void* q, float q_scale,
+                                    const void* k_cache, const void* v_cache,
+                                    const void* k_scales, const void* v_scales,
+                                    const int32_t* page_table, const int32_t* idx, float* partial,
+                                    int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                    void* workspace, sps_stream_t stream);
+
+/*
  * sps_kv_append -- the chunked-prefill step before indexer_scores: writes the batch's new
  * tokens' K and V into the paged cache (the formats of "MSA PR 21: Q8KV4 paged sparse
  * prefill": E4M3 query, NVFP4 K/V with an E4M3 scale per 16 elements; the pages fix no

@@ -19,7 +19,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "liboracle.so")
 _SRC = os.path.join(_HERE, "oracle.c")
 
-DTYPES = {"bf16": 0, "fp16": 1, "e4m3": 2, "nvfp4": 3, "fp32": 4}
+DTYPES = {"bf16": 0, "fp16": 1, "e4m3": 2, "nvfp4": 3, "fp32": 4, "nvfp4_e4m3": 5}
 
 
 def build(force: bool = False) -> str:
@@ -105,6 +105,7 @@ class Tensor:
 
     ``data``: uint16 (bf16/fp16), uint8 (e4m3), packed uint8 codes (nvfp4, even element in
     the low nibble) or float32.  ``scales``: uint8 E4M3, one per 16 elements (nvfp4 only).
+    ``nvfp4_e4m3``: NVFP4 whose code x scale products are rounded to E4M3 (the pages' QMUL4).
     ``scale``: per-tensor multiplier applied after decoding.
     """
 
@@ -224,7 +225,7 @@ def num_threads() -> int:
 def decode(t: Tensor, first: int = 0, n: int | None = None) -> np.ndarray:
     """Decoded values (times the per-tensor scale) of n elements starting at ``first``."""
     if n is None:
-        n = t.data.size * (2 if t.dtype == "nvfp4" else 1) - first
+        n = t.data.size * (2 if t.dtype.startswith("nvfp4") else 1) - first
     out = np.empty(n, dtype=np.float64)
     lib().orc_decode(t.c(), first, n, _ptr(out))
     return out

@@ -86,6 +86,7 @@ def lib(path: str | None = None):
     L.sparse_prefill_fwd.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
     L.partial_combine.argtypes = [i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, vp, vp]
     L.sparse_prefill_fwd_bf16.argtypes = L.sparse_prefill_fwd.argtypes
+    L.sparse_prefill_fwd_fp8qk.argtypes = L.sparse_prefill_fwd.argtypes
     L.sps_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.sps_quantize_e4m3.argtypes = [vp, i64, f32, vp, vp]
     L.sps_absmax_bf16.argtypes = [vp, i64, vp, vp]
@@ -194,6 +195,16 @@ def sparse_prefill_fwd_bf16(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, 
                                          _ptr(page_table), _ptr(idx), _ptr(partial),
                                          partial.stride(0), _ptr(lse), lse.stride(0),
                                          _ptr(workspace), _stream(stream)))
+
+
+def sparse_prefill_fwd_fp8qk(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
+                             page_table, idx, partial, lse, workspace, stream=None):
+    """As ``sparse_prefill_fwd``: E4M3 Q, NVFP4 K rounded to E4M3, FP8 Q K^T (the pages' route)."""
+    _check(lib().sparse_prefill_fwd_fp8qk(plan.handle, _ptr(q), float(q_scale), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                          _ptr(page_table), _ptr(idx), _ptr(partial),
+                                          partial.stride(0), _ptr(lse), lse.stride(0),
+                                          _ptr(workspace), _stream(stream)))
 
 
 def sparse_prefill_fwd_noalloc(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,

@@ -75,7 +75,44 @@ nvfp4_to_f16_kernel(const uint2* __restrict__ codes, const uint8_t* __restrict__
   }
 }
 
+// One NVFP4 block -> 16 E4M3 codes: the exact FP16 product, then cvt.rn.satfinite to E4M3.
+__global__ void __launch_bounds__(256)
+nvfp4_to_e4m3_kernel(const uint2* __restrict__ codes, const uint8_t* __restrict__ scales,
+                     uint4* __restrict__ out, int64_t nblocks) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblocks;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint2 c = __ldg(codes + i);
+    const uint8_t sb = __ldg(scales + i);
+    const uint32_t s2 = cvt_e4m3x2((uint16_t)(sb | (sb << 8)));
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int b = 0; b < 4; b += 2) {
+        const uint32_t h0 = hmul2_u32(cvt_e2m1x2((uint16_t)((w[j] >> (8 * b)) & 0xff)), s2);
+        const uint32_t h1 = hmul2_u32(cvt_e2m1x2((uint16_t)((w[j] >> (8 * b + 8)) & 0xff)), s2);
+        uint16_t e0, e1;
+        asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e0) : "r"(h0));
+        asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e1) : "r"(h1));
+        o[2 * j + b / 2] = (uint32_t)e0 | ((uint32_t)e1 << 16);
+      }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_e4m3(const void* in, const void* scales, int64_t n, void* out,
+                                cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = n / 16;
+  const unsigned grid = (unsigned)std::min<int64_t>((blocks + 255) / 256, 8LL * num_sms());
+  nvfp4_to_e4m3_kernel<<<grid, 256, 0, st>>>(static_cast<const uint2*>(in),
+                                              static_cast<const uint8_t*>(scales),
+                                              static_cast<uint4*>(out), blocks);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
                            void* out, cudaStream_t st) {

@@ -41,17 +41,23 @@ namespace {
 
 constexpr int kThreads = 512;   // 4 warpgroups
 
+// Operand modes: kModeBF16 (Q, K, V BF16), kModeF16 (Q, K, V FP16, the exact dequantised
+// NVFP4 path), kModeFP8QK (Q and K E4M3 bytes, S on the FP8 tensor core; V FP16).
+constexpr int kModeBF16 = 0, kModeF16 = 1, kModeFP8QK = 2;
+
 // PB16: partials are stored as BF16 instead of FP32.  The staging rows then take half the
-// space, which leaves room for a third Q stage.
-template <int D, bool PB16>
+// space, which leaves room for a third Q stage; E4M3 Q rows are half as wide again.
+template <int D, int MODE, bool PB16>
 struct FwdSmem {
-  static constexpr int TILE = 128 * D * 2;  // 128 rows of D 16-bit elements
-  static constexpr int QS = PB16 ? 3 : 2;   // Q ring stages
+  static constexpr int QE = MODE == kModeFP8QK ? 1 : 2;  // bytes per Q / K element
+  static constexpr int TQK = 128 * D * QE;  // 128-row Q or K tile
+  static constexpr int TV = 128 * D * 2;    // 128-row V tile (16-bit)
+  static constexpr int QS = MODE == kModeFP8QK ? 4 : (PB16 ? 3 : 2);  // Q ring stages
   static constexpr int PE = PB16 ? 2 : 4;   // bytes per partial element
   static constexpr int SRB = D * PE + 16;   // staging row bytes (pad: conflict-free writes)
-  uint8_t k[TILE];
-  uint8_t v[TILE];
-  uint8_t q[QS][TILE];
+  uint8_t k[TQK];
+  uint8_t v[TV];
+  uint8_t q[QS][TQK];
   alignas(16) uint8_t stage[128 * SRB];  // one O row per epilogue thread
   float inv_l[2][128];
   int2 rs[2][128];
@@ -63,9 +69,9 @@ struct FwdSmem {
   int abort_flag;
 };
 
-// F16IN: Q, K and V arrive as FP16 (dequantised inputs) instead of BF16; then S = Q K^T runs
-// on FP16 operands and V needs no conversion.  PB16: BF16 partials (see FwdSmem).
-template <int D, bool F16IN, bool PB16>
+// MODE: see above; with FP16 or E4M3 operands V arrives as FP16 and needs no conversion.
+// PB16: BF16 partials (see FwdSmem).
+template <int D, int MODE, bool PB16>
 __global__ void __launch_bounds__(kThreads, 1)
 forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -73,12 +79,16 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
                const int32_t* __restrict__ page_table, void* __restrict__ partial,
                int64_t split_stride, float* __restrict__ lse, int64_t lse_split_stride,
                float q_scale) {
-  using Smem = FwdSmem<D, PB16>;
+  using Smem = FwdSmem<D, MODE, PB16>;
+  constexpr bool F16IN = MODE != kModeBF16;  // V is FP16
+  constexpr bool FP8QK = MODE == kModeFP8QK;
   constexpr int kQS = Smem::QS;
-  constexpr int DB = D / 64;          // 128-byte column blocks of a 16-bit row
-  constexpr int TILE = Smem::TILE;
-  constexpr int QK_STEPS = D / 16;
-  constexpr uint32_t IDESC_QK = idesc_mma(!F16IN, !F16IN, 128, 128, false, false);
+  constexpr int DB = D / 64;          // 128-byte column blocks of a 16-bit (V) row
+  constexpr int DBQ = D * Smem::QE / 128;  // 128-byte column blocks of a Q / K row
+  constexpr int TQK = Smem::TQK, TILE = Smem::TV;
+  constexpr int QK_STEPS = D * Smem::QE / 32;  // one MMA per 32 bytes of K depth
+  constexpr uint32_t IDESC_QK = idesc_mma(MODE == kModeBF16, MODE == kModeBF16, 128, 128, false,
+                                          false);
   constexpr uint32_t IDESC_PV = idesc_mma(false, false, 128, D, false, true);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -145,9 +155,9 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       // K as soon as the previous item's last S has read the old tile, V after its last P.V
       if (!mbar_wait(smem_u32(&sm.k_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
       const uint32_t kf = smem_u32(&sm.k_full);
-      mbar_expect_tx(kf, TILE);
-      for (int db = 0; db < DB; ++db)
-        tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * 64, krow, kf);
+      mbar_expect_tx(kf, TQK);
+      for (int db = 0; db < DBQ; ++db)
+        tma_load_2d(smem_u32(sm.k) + db * 16384, &tmK, db * (128 / Smem::QE), krow, kf);
       if (!mbar_wait(smem_u32(&sm.v_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;
       const uint32_t vf = smem_u32(&sm.v_full);
       mbar_expect_tx(vf, TILE);
@@ -210,8 +220,12 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
 #pragma unroll
             for (int kk = 0; kk < QK_STEPS; ++kk) {
               const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-              mma_f16_ss(tmem + b * 128, sdesc_sw128(qb + off, 16, 1024),
-                         sdesc_sw128(kb + off, 16, 1024), IDESC_QK, kk > 0);
+              if (FP8QK)
+                mma_f8_ss(tmem + b * 128, sdesc_sw128(qb + off, 16, 1024),
+                          sdesc_sw128(kb + off, 16, 1024), IDESC_QK, kk > 0);
+              else
+                mma_f16_ss(tmem + b * 128, sdesc_sw128(qb + off, 16, 1024),
+                           sdesc_sw128(kb + off, 16, 1024), IDESC_QK, kk > 0);
             }
             mma_commit(smem_u32(&sm.s_full[b]));
             mma_commit(smem_u32(&sm.q_empty[qs]));
@@ -450,7 +464,7 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
     // op = 8 DB w + l, column block op / 32, group rows 4 (op % 32) .. +3 (rows past the end
     // of the group repeat its first row).  The indices of group g+1 are fetched while g is
     // issued.
-    const int nops = 8 * DB;
+    const int nops = 8 * DBQ;
     const int op = (warp - 12) * nops + lane;
     const int db = op / 32, quad = op % 32;
     const bool active = lane < nops;
@@ -497,11 +511,12 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
       const uint32_t qf = smem_u32(&sm.q_full[qs]);
       if (lane == 0) {
         ok = mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQS) & 1) ^ 1, abort_flag, status);
-        if (ok) mbar_expect_tx(qf, TILE / 4);
+        if (ok) mbar_expect_tx(qf, TQK / 4);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (active)
-        tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + quad * 512, &tmQ, db * 64, rows[0],
+        tma_gather4_hint(smem_u32(sm.q[qs]) + db * 16384 + quad * 512, &tmQ,
+                         db * (128 / Smem::QE), rows[0],
                          rows[1], rows[2], rows[3], qf, pol_q);
       ++q_it;
       ti = ti2;
@@ -517,20 +532,25 @@ forward_kernel(const void* __restrict__ q, const __grid_constant__ CUtensorMap t
   }
 }
 
-template <int D, bool F16IN, bool PB16>
+template <int D, int MODE, bool PB16>
 cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const void* vc,
                         const int32_t* page_table, void* partial, int64_t split_stride,
                         float* lse, int64_t lse_split_stride, float q_scale, cudaStream_t st) {
   alignas(64) CUtensorMap tmQ, tmK, tmV;
   const uint64_t R = (uint64_t)p.T * p.H;
   const uint64_t kv_rows = (uint64_t)p.num_phys * p.Hkv * 128;
-  const int dt = F16IN ? 1 : 0;  // tensor-map element type: BF16 or FP16
-  if (!encode_tmap_2d(&tmQ, dt, const_cast<void*>(q), D, R, (uint64_t)D * 2, 64, 1, true) ||
-      !encode_tmap_2d(&tmK, dt, const_cast<void*>(kc), D, kv_rows, (uint64_t)D * 2, 64, 128, true) ||
-      !encode_tmap_2d(&tmV, dt, const_cast<void*>(vc), D, kv_rows, (uint64_t)D * 2, 64, 128, true))
+  // tensor-map element types: BF16 (0), FP16 (1) or bytes (2); Q and K rows of 128 bytes
+  const int dqk = MODE == kModeBF16 ? 0 : (MODE == kModeF16 ? 1 : 2);
+  const int dv = MODE == kModeBF16 ? 0 : 1;
+  const uint64_t qe = MODE == kModeFP8QK ? 1 : 2;
+  const uint32_t box_qk = (uint32_t)(128 / qe);
+  if (!encode_tmap_2d(&tmQ, dqk, const_cast<void*>(q), D, R, (uint64_t)D * qe, box_qk, 1, true) ||
+      !encode_tmap_2d(&tmK, dqk, const_cast<void*>(kc), D, kv_rows, (uint64_t)D * qe, box_qk, 128,
+                      true) ||
+      !encode_tmap_2d(&tmV, dv, const_cast<void*>(vc), D, kv_rows, (uint64_t)D * 2, 64, 128, true))
     return cudaErrorInvalidValue;
-  const int smem = (int)sizeof(FwdSmem<D, PB16>) + 1024;
-  auto kern = forward_kernel<D, F16IN, PB16>;
+  const int smem = (int)sizeof(FwdSmem<D, MODE, PB16>) + 1024;
+  auto kern = forward_kernel<D, MODE, PB16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreads, smem, st>>>(q, tmQ, tmK, tmV, p, page_table, partial, split_stride,
@@ -543,13 +563,25 @@ cudaError_t launch_forward_t(const DevPlan& p, sps_dtype qt, sps_dtype kvt, cons
                              float q_scale, const void* kc, const void* vc, const void* ks,
                              const void* vs, const int32_t* page_table, void* partial,
                              int64_t split_stride, float* lse, int64_t lse_split_stride,
-                             cudaStream_t st) {
+                             bool fp8qk, cudaStream_t st) {
+  if (fp8qk) {
+    // the pages' Q8KV4 route: E4M3 Q as given, K = NVFP4 products rounded to E4M3, S on the
+    // FP8 tensor core; V exact in FP16 for P.V
+    if (qt != SPS_E4M3 || kvt != SPS_NVFP4 || p.D != 128) return cudaErrorNotSupported;
+    if (!p.kconv || !p.vconv) return cudaErrorInvalidValue;
+    const int64_t ce = (int64_t)p.num_phys * p.Hkv * 128 * p.D;
+    cudaError_t e = launch_dequant_e4m3(kc, ks, ce, p.kconv, st);
+    if (e == cudaSuccess) e = launch_dequant(SPS_NVFP4, vc, vs, ce, p.vconv, st);
+    if (e != cudaSuccess) return e;
+    return run_forward<128, kModeFP8QK, PB16>(p, q, p.kconv, p.vconv, page_table, partial,
+                                              split_stride, lse, lse_split_stride, q_scale, st);
+  }
   if (qt == SPS_BF16 && kvt == SPS_BF16) {
     if (p.D == 128)
-      return run_forward<128, false, PB16>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                                           lse_split_stride, q_scale, st);
-    return run_forward<64, false, PB16>(p, q, kc, vc, page_table, partial, split_stride, lse,
-                                        lse_split_stride, q_scale, st);
+      return run_forward<128, kModeBF16, PB16>(p, q, kc, vc, page_table, partial, split_stride,
+                                               lse, lse_split_stride, q_scale, st);
+    return run_forward<64, kModeBF16, PB16>(p, q, kc, vc, page_table, partial, split_stride, lse,
+                                            lse_split_stride, q_scale, st);
   }
   if (qt == SPS_E4M3 && kvt == SPS_NVFP4) {
     // exact FP16 copies of the E4M3 codes and of the NVFP4 products; q_scale stays in the
@@ -561,10 +593,10 @@ cudaError_t launch_forward_t(const DevPlan& p, sps_dtype qt, sps_dtype kvt, cons
     if (e == cudaSuccess) e = launch_dequant(SPS_NVFP4, vc, vs, ce, p.vconv, st);
     if (e != cudaSuccess) return e;
     if (p.D == 128)
-      return run_forward<128, true, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
-                                          split_stride, lse, lse_split_stride, q_scale, st);
-    return run_forward<64, true, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
-                                       split_stride, lse, lse_split_stride, q_scale, st);
+      return run_forward<128, kModeF16, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
+                                              split_stride, lse, lse_split_stride, q_scale, st);
+    return run_forward<64, kModeF16, PB16>(p, p.qconv, p.kconv, p.vconv, page_table, partial,
+                                           split_stride, lse, lse_split_stride, q_scale, st);
   }
   return cudaErrorNotSupported;
 }
@@ -577,7 +609,7 @@ cudaError_t launch_forward(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const 
                            int64_t split_stride, float* lse, int64_t lse_split_stride,
                            cudaStream_t st) {
   return launch_forward_t<false>(p, qt, kvt, q, q_scale, kc, vc, ks, vs, page_table, partial,
-                                 split_stride, lse, lse_split_stride, st);
+                                 split_stride, lse, lse_split_stride, false, st);
 }
 
 cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
@@ -586,7 +618,16 @@ cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, 
                                  int64_t split_stride, float* lse, int64_t lse_split_stride,
                                  cudaStream_t st) {
   return launch_forward_t<true>(p, qt, kvt, q, q_scale, kc, vc, ks, vs, page_table, partial,
-                                split_stride, lse, lse_split_stride, st);
+                                split_stride, lse, lse_split_stride, false, st);
+}
+
+cudaError_t launch_forward_fp8qk(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                                 float q_scale, const void* kc, const void* vc, const void* ks,
+                                 const void* vs, const int32_t* page_table, float* partial,
+                                 int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                 cudaStream_t st) {
+  return launch_forward_t<false>(p, qt, kvt, q, q_scale, kc, vc, ks, vs, page_table, partial,
+                                 split_stride, lse, lse_split_stride, true, st);
 }
 
 }  // namespace sps

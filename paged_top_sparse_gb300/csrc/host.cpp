@@ -400,12 +400,14 @@ sps_status topk_select(const sps_plan* pl, const float* scores, int64_t score_pi
 
 namespace {
 
-// The forward with FP32 (bf16p = false) or BF16 partials: the same checks and launches.
+// The forward with FP32 or BF16 partials, or the FP8-QK route: the same checks and launches.
+enum class FwdKind { kFP32, kBF16Partials, kFP8QK };
 sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const void* k_cache,
                       const void* v_cache, const void* k_scales, const void* v_scales,
                       const int32_t* page_table, const int32_t* idx, void* partial,
                       int64_t split_stride, float* lse, int64_t lse_split_stride, void* ws,
-                      sps_stream_t stream, bool bf16p) {
+                      sps_stream_t stream, FwdKind kind) {
+  const bool bf16p = kind == FwdKind::kBF16Partials;
   sps_status st = check_plan_ws(pl, ws);
   if (st != SPS_OK) return st;
   const sps_problem& p = pl->pb;
@@ -423,6 +425,9 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
                 (long long)qa);
   if (lse_split_stride < pl->R) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
   if (!std::isfinite(q_scale)) return fail(SPS_EINVAL, "q_scale must be finite");
+  if (kind == FwdKind::kFP8QK &&
+      (p.q_dtype != SPS_E4M3 || p.kv_dtype != SPS_NVFP4 || p.head_dim != 128))
+    return fail(SPS_EUNSUPPORTED, "sparse_prefill_fwd_fp8qk: needs E4M3 Q, NVFP4 K/V, D = 128");
   DevPlan d = make_dev_plan(pl, ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // counters [1] (forward task cursor) and [2] (task count) start at zero
@@ -430,6 +435,12 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
   e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
+  if (kind == FwdKind::kFP8QK)
+    return launched(launch_forward_fp8qk(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
+                                         k_scales, v_scales, page_table,
+                                         static_cast<float*>(partial), split_stride, lse,
+                                         lse_split_stride, s),
+                    "forward launch");
   if (bf16p)
     return launched(launch_forward_bf16p(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
                                          k_scales, v_scales, page_table, partial, split_stride,
@@ -480,7 +491,17 @@ sps_status sparse_prefill_fwd(const sps_plan* pl, const void* q, float q_scale,
                               float* lse, int64_t lse_split_stride, void* ws,
                               sps_stream_t stream) {
   return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
-                    partial, split_stride, lse, lse_split_stride, ws, stream, false);
+                    partial, split_stride, lse, lse_split_stride, ws, stream, FwdKind::kFP32);
+}
+
+sps_status sparse_prefill_fwd_fp8qk(const sps_plan* pl, const void* q, float q_scale,
+                                    const void* k_cache, const void* v_cache,
+                                    const void* k_scales, const void* v_scales,
+                                    const int32_t* page_table, const int32_t* idx, float* partial,
+                                    int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                    void* ws, sps_stream_t stream) {
+  return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
+                    partial, split_stride, lse, lse_split_stride, ws, stream, FwdKind::kFP8QK);
 }
 
 sps_status sparse_prefill_fwd_bf16(const sps_plan* pl, const void* q, float q_scale,
@@ -490,7 +511,8 @@ sps_status sparse_prefill_fwd_bf16(const sps_plan* pl, const void* q, float q_sc
                                    void* partial_bf16, int64_t split_stride, float* lse,
                                    int64_t lse_split_stride, void* ws, sps_stream_t stream) {
   return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
-                    partial_bf16, split_stride, lse, lse_split_stride, ws, stream, true);
+                    partial_bf16, split_stride, lse, lse_split_stride, ws, stream,
+                    FwdKind::kBF16Partials);
 }
 
 sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const float* partial,

@@ -90,6 +90,12 @@ cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, 
                                  const void* vs, const int32_t* page_table, void* partial,
                                  int64_t split_stride, float* lse, int64_t lse_split_stride,
                                  cudaStream_t st);
+// The pages' Q8KV4 route: K rounded to E4M3, S = Q K^T on the FP8 tensor core (D = 128).
+cudaError_t launch_forward_fp8qk(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                                 float q_scale, const void* kc, const void* vc, const void* ks,
+                                 const void* vs, const int32_t* page_table, float* partial,
+                                 int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                 cudaStream_t st);
 // The combine over BF16 partials.
 cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const void* partial,
                                  int64_t split_stride, const float* lse, int64_t lse_split_stride,
@@ -111,6 +117,10 @@ cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t 
 // Exact E4M3 / NVFP4 -> FP16 conversion of n elements (n % 16 == 0).
 cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
                            void* out, cudaStream_t st);
+// NVFP4 -> E4M3 codes: each exact code x scale product rounded to nearest even E4M3
+// (saturating), the pages' QMUL4 dequant.
+cudaError_t launch_dequant_e4m3(const void* in, const void* scales, int64_t n, void* out,
+                                cudaStream_t st);
 
 // Tensor-map encoding through the driver entry point (no link against libcuda).
 bool encode_tmap_2d(void* map, int dtype_code, void* base, uint64_t inner, uint64_t outer,

@@ -402,6 +402,45 @@ def test_bf16_partials_path(name):
     assert rel_l2(got, ref) <= tol[0] and np.max(np.abs(got - ref)) <= tol[1]
 
 
+@pytest.mark.parametrize("name", ["quant_small", "prefill8k_q"])
+def test_fp8qk_route_matches_oracle_on_e4m3_rounded_keys(name):
+    """sparse_prefill_fwd_fp8qk (the pages' Q8KV4 route: K products rounded to E4M3, FP8 Q K^T)
+    against the oracle decoding K the same way (the 'nvfp4_e4m3' tensor): partials and LSE at
+    the exact path's tolerances, the combined output at the quantised-input bound.  The
+    distance to the exact-product oracle is reported by the second check, whose bound is the
+    rounding of K to E4M3 (3 mantissa bits) seen through the softmax."""
+    from paged_top_sparse_gb300 import binding as B
+
+    r = _run(name)
+    w, run, rows = r["w"], r["run"], r["rows"]
+    R, K, D = w.num_rows, w.top_k, w.head_dim
+    dev = run.dev
+    part = torch.full((K, R, D), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((K, R), float("nan"), dtype=torch.float32, device=dev)
+    B.sparse_prefill_fwd_fp8qk(run.plan, run.q, run.q_scale, run.k, run.v, run.k_scales,
+                               run.v_scales, run.page_table, run.idx, part, lse, run.ws)
+    out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    B.partial_combine(part, lse, out)
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    rows_t = torch.from_numpy(rows).to(dev)
+    q, k, v, qi, ki = oracle_tensors(w, r["t"])
+    kr = orc.Tensor(k.data, "nvfp4_e4m3", scales=k.scales, scale=k.scale)
+    pb = oracle_problem(w)
+    ref_p, ref_l = orc.forward(pb, q, kr, v, w.sm_scale, r["idx"], rows)
+    got_p = part[:, rows_t].cpu().numpy().transpose(1, 0, 2)
+    got_l = lse[:, rows_t].cpu().numpy().T
+    live = r["idx"] >= 0
+    assert rel_l2(got_p[live], ref_p[live]) <= PARTIAL_RL2
+    assert np.max(np.abs(got_l[live] - ref_l[live])) <= LSE_ATOL
+    got = out[rows_t].float().cpu().numpy()
+    ref, _ = orc.dense(pb, q, kr, v, w.sm_scale, r["idx"], rows)
+    tol = OUT_TOL["quant"]
+    assert rel_l2(got, ref) <= tol[0] and np.max(np.abs(got - ref)) <= tol[1]
+    exact, _ = orc.dense(pb, q, k, v, w.sm_scale, r["idx"], rows)
+    assert rel_l2(got, exact) <= 5e-2
+
+
 def test_bad_page_table_entry_sets_status():
     """An out-of-range physical page is caught on the device: status, no fault."""
     from tests.gpu_helpers import DeviceRun

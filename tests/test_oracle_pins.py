@@ -481,3 +481,20 @@ def test_kv_append_places_tokens_through_page_table():
             assert np.array_equal(scl[phys, :, t % P], qs[tk])
             tk += 1
     assert not codes[~written].any() and not scl[~written].any()
+
+
+def test_nvfp4_e4m3_rounded_decode_is_nearest_e4m3_of_the_product():
+    """The 'nvfp4_e4m3' decode (the pages' QMUL4 dequant) gives, for every one of the 16 x 127
+    (code, scale) pairs, torch's float8_e4m3fn rounding of the exact product, and +-448 where
+    the product lies beyond the E4M3 range (saturating conversion)."""
+    scale_codes = np.arange(0, 0x7F, dtype=np.uint8)
+    nibs = np.arange(16, dtype=np.uint8)
+    codes = np.repeat((nibs[0::2] | (nibs[1::2] << 4))[None, :], len(scale_codes), 0).reshape(-1)
+    scales = np.repeat(scale_codes, 1)  # one scale per 16-element block = per row of 8 bytes
+    exact = orc.decode(orc.Tensor(codes, "nvfp4", scales=scales))
+    rounded = orc.decode(orc.Tensor(codes, "nvfp4_e4m3", scales=scales))
+    inr = np.abs(exact) <= 448  # torch's cast gives NaN beyond the E4M3 range; ours saturates
+    want = torch.from_numpy(exact[inr].astype(np.float32)).to(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(rounded[inr], want.astype(np.float64))
+    assert np.all(rounded[~inr] == np.sign(exact[~inr]) * 448.0) and (~inr).any()
+    assert np.any(rounded[inr] != exact[inr])  # some products need rounding (6 significant bits)
