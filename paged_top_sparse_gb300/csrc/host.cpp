@@ -50,11 +50,11 @@ struct sps_plan {
   std::vector<int32_t> page_req;  // [total_pages]
   std::vector<IdxTask> idx_tasks;
   int64_t T = 0, R = 0, num_buckets = 0, max_entries = 0, max_fwd_tasks = 0;
-  int64_t total_pages = 0, bm_total_words = 0, num_chunks = 0;
+  int64_t total_pages = 0, num_chunks = 0, inv_blocks = 0;
   // workspace layout (bytes)
   int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
-          off_page_req = 0, off_idx_tasks = 0, off_bitmap = 0, off_chunk_offsets = 0,
-          off_word_pos = 0, off_qconv = -1, off_kconv = -1, off_vconv = -1,
+          off_page_req = 0, off_idx_tasks = 0, off_chunk_offsets = 0,
+          off_qconv = -1, off_kconv = -1, off_vconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
   int64_t upload_bytes = 0;  // [off_tok_pos, off_tok_pos + upload_bytes) comes from `blob`
   std::vector<uint8_t> blob;
@@ -176,7 +176,7 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
 
   // per-request info, per-token metadata
   std::vector<int32_t> tok_pos, tok_req;
-  int32_t tok = 0, page_base = 0, bm_base = 0;
+  int32_t tok = 0, page_base = 0;
   for (int b = 0; b < p.batch; ++b) {
     ReqInfo ri{};
     ri.tok0 = tok;
@@ -184,9 +184,10 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
     ri.ctx = pl->ctx_lens[b];
     ri.npages = ri.q_len > 0 ? (ri.ctx + ri.q_len - 1) / kPage + 1 : 0;
     ri.page_base = page_base;
-    ri.bm_words = (int32_t)((int64_t(ri.q_len) * Hg + 31) / 32);
-    ri.bm_base = bm_base;
-    ri.ch_per_bucket = (ri.bm_words + kChunkWords - 1) / kChunkWords;
+    ri.words = (int32_t)((int64_t(ri.q_len) * Hg + 31) / 32);
+    ri.ch_per_bucket = (ri.words + kChunkWords - 1) / kChunkWords;
+    ri.blk_base = (int32_t)pl->inv_blocks;
+    pl->inv_blocks += (int64_t)p.num_kv_heads * ri.ch_per_bucket;
     ri.ch_base = (int32_t)pl->num_chunks;
     pl->num_chunks += (int64_t)ri.npages * p.num_kv_heads * ri.ch_per_bucket;
     for (int i = 0; i < ri.q_len; ++i) {
@@ -194,7 +195,6 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
       tok_req.push_back(b);
     }
     for (int pg = 0; pg < ri.npages; ++pg) pl->page_req.push_back(b);
-    bm_base += ri.npages * p.num_kv_heads * ri.bm_words;
     page_base += ri.npages;
     tok += ri.q_len;
     pl->reqs.push_back(ri);
@@ -203,7 +203,6 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->R = (int64_t)tok * p.num_q_heads;
   pl->total_pages = page_base;
   pl->num_buckets = (int64_t)page_base * p.num_kv_heads;
-  pl->bm_total_words = bm_base;
   pl->max_entries = pl->R * p.top_k;
   const int64_t per_task = (int64_t)kFwdTaskGroups * 128;
   pl->max_fwd_tasks = pl->max_entries / per_task + pl->num_buckets + 1;
@@ -224,9 +223,7 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->off_page_req = take(4 * std::max<int64_t>(1, pl->total_pages));
   pl->off_idx_tasks = take(sizeof(IdxTask) * std::max<size_t>(1, pl->idx_tasks.size()));
   int64_t upload_end = off;
-  pl->off_bitmap = take(4 * std::max<int64_t>(1, pl->bm_total_words));
   pl->off_chunk_offsets = take(4 * (pl->num_chunks + 1));
-  pl->off_word_pos = take(4 * std::max<int64_t>(1, pl->bm_total_words));
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
@@ -299,9 +296,7 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.max_fwd_tasks = (int32_t)pl->max_fwd_tasks;
   d.n_idx_tasks = (int32_t)pl->idx_tasks.size();
   d.total_pages = (int32_t)pl->total_pages;
-  d.bm_total_words = (int32_t)pl->bm_total_words;
-  d.mark_warps = 0;
-  for (const ReqInfo& ri : pl->reqs) d.mark_warps += (int64_t)p.num_kv_heads * ri.bm_words;
+  d.inv_blocks = (int32_t)pl->inv_blocks;
   d.sm_scale = p.softmax_scale;
   d.status = reinterpret_cast<int32_t*>(base + pl->off_status);
   d.counters = reinterpret_cast<int32_t*>(base + pl->off_counters);
@@ -310,10 +305,8 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.reqs = reinterpret_cast<const ReqInfo*>(base + pl->off_reqs);
   d.page_req = reinterpret_cast<const int32_t*>(base + pl->off_page_req);
   d.idx_tasks = reinterpret_cast<const IdxTask*>(base + pl->off_idx_tasks);
-  d.bitmap = reinterpret_cast<uint32_t*>(base + pl->off_bitmap);
   d.num_chunks = (int32_t)pl->num_chunks;
   d.chunk_offsets = reinterpret_cast<int32_t*>(base + pl->off_chunk_offsets);
-  d.word_pos = reinterpret_cast<int32_t*>(base + pl->off_word_pos);
   d.bucket_offsets = reinterpret_cast<int32_t*>(base + pl->off_bucket_offsets);
   d.entries = reinterpret_cast<int2*>(base + pl->off_entries);
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
@@ -430,8 +423,9 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
     return fail(SPS_EUNSUPPORTED, "sparse_prefill_fwd_fp8qk: needs E4M3 Q, NVFP4 K/V, D = 128");
   DevPlan d = make_dev_plan(pl, ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // counters [1] (forward task cursor) and [2] (task count) start at zero
-  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 2 * sizeof(int32_t), s);
+  // counters [1] (forward task cursor), [2] (task count) and [3] (inversion buckets scanned)
+  // start at zero
+  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 3 * sizeof(int32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
   e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");

@@ -3,19 +3,22 @@
 // The forward runs one work item per (page, KV head, query split) ("MSA PR 21: Q8KV4 paged
 // sparse prefill", K1), so the row-major selection idx[row][slot] is turned around: for every
 // bucket (request, logical page, KV head) the (row, slot) pairs that chose it, in ascending row
-// order.  Nothing depends on the timing of atomics:
+// order.  Nothing depends on the timing of atomics, and no global atomics are used:
 //
-//   1. mark     a warp per 32 consecutive rows of one (request, KV head) sets one bit per
-//               (bucket, row) in a selection bitmap (each bucket owns a run of words, bit b
-//               of word w = row 32 w + b); warp-aggregated atomicOr; empty slots get
-//               lse = -inf here.
-//   2. count    a block per 2048-word chunk of a bucket: popcount of the chunk.
-//   3. scan     one block: exclusive scan over chunks (buckets are runs of chunks) gives each
-//               chunk's first entry and each bucket's CSR offset; then the forward's work
-//               list (chunks of up to kFwdTaskGroups x 128 entries per bucket).
-//   4. prefix   a block per chunk: exclusive popcount scan -> first entry of every word.
-//   5. emit     a warp per 32 rows again: for every (row, slot) the entry position is the
-//               word's first entry plus the set bits below the row's bit.  An entry is
+//   1. count    a 256-thread block per (request, KV head, chunk of 256 consecutive rows of
+//               the group), a thread per row.  Per window of 64 pages each thread turns its
+//               row's selection (read as 16-byte vectors when top_k allows) into a 64-bit page
+//               mask, and 64 ballots turn a warp's 32 masks around into one 32-bit row mask per
+//               page; the block sums the popcounts of each page's 8 warp masks into that
+//               (bucket, chunk)'s entry count.  Empty slots get lse = -inf here.
+//   2. chunks   a block per bucket: exclusive scan over the bucket's chunks (bucket-local
+//               offsets) and the bucket's total.  The last block to finish (an atomic ticket
+//               after a memory fence, no waiting) then runs
+//   3. buckets  exclusive scan over the bucket totals, which gives the CSR offsets, and the
+//               forward's work list (chunks of up to kFwdTaskGroups x 128 entries per bucket).
+//   4. emit     the grid of step 1 rebuilds the same masks; a page's entries of the chunk
+//               start at the bucket's offset plus the chunk's plus the rows of earlier warps,
+//               and a row's entry at that plus the set bits of lower lanes.  An entry is
 //               (row, t * 64 + slot), t the row's absolute position, so the forward needs no
 //               further lookup to find the row's own page and visible key count.
 #include "ptx.cuh"
@@ -24,39 +27,26 @@
 namespace sps {
 namespace {
 
-// Warp wid of the mark/emit grids -> request, KV head and bitmap word index.
-__device__ __forceinline__ int find_word(const DevPlan& p, int64_t wid, int* w_in_req, int* g) {
-  int64_t acc = 0;
+// Block of steps 1 and 3 -> request, KV head and chunk of the bucket.  Returns -1 if none.
+__device__ __forceinline__ int find_block(const DevPlan& p, int blk, int* g, int* c) {
   for (int b = 0; b < p.batch; ++b) {
-    const int nw = p.reqs[b].bm_words;
-    const int64_t n = (int64_t)p.Hkv * nw;
-    if (wid < acc + n) {
-      const int64_t local = wid - acc;
-      *g = (int)(local / nw);
-      *w_in_req = (int)(local % nw);
+    const ReqInfo& ri = p.reqs[b];
+    const int n = p.Hkv * ri.ch_per_bucket;
+    if (blk < ri.blk_base + n) {
+      if (blk < ri.blk_base) return -1;
+      const int local = blk - ri.blk_base;
+      *g = local / ri.ch_per_bucket;
+      *c = local % ri.ch_per_bucket;
       return b;
     }
-    acc += n;
   }
   return -1;
 }
 
-// Chunk id -> request, bucket, bucket-local (page, kv head) and chunk-within-bucket.
-__device__ __forceinline__ int find_chunk(const DevPlan& p, int chunk, int* bucket, int* pg,
-                                          int* g, int* c) {
-  for (int b = p.batch - 1; b >= 0; --b) {
-    const ReqInfo& ri = p.reqs[b];
-    if (ri.npages > 0 && chunk >= ri.ch_base) {
-      const int lc = chunk - ri.ch_base;
-      const int bl = lc / ri.ch_per_bucket;
-      *c = lc % ri.ch_per_bucket;
-      *pg = bl / p.Hkv;
-      *g = bl % p.Hkv;
-      *bucket = (ri.page_base + *pg) * p.Hkv + *g;
-      return b;
-    }
-  }
-  return -1;
+// Chunk c of bucket (page pg of request ri, KV head g).
+__device__ __forceinline__ int chunk_id(const DevPlan& p, const ReqInfo& ri, int pg, int g,
+                                        int c) {
+  return ri.ch_base + (pg * p.Hkv + g) * ri.ch_per_bucket + c;
 }
 
 struct RowCtx {
@@ -66,11 +56,12 @@ struct RowCtx {
   int o;  // its own page
 };
 
+// Row of lane `lane` in 32-row word w of KV group g of request ri.
 __device__ __forceinline__ RowCtx row_of(const DevPlan& p, const ReqInfo& ri, int g, int w,
                                          int lane) {
   RowCtx rc;
   const int row_local = w * 32 + lane;
-  rc.valid = row_local < ri.q_len * p.Hg;
+  rc.valid = w < ri.words && row_local < ri.q_len * p.Hg;
   rc.r = 0;
   rc.t = 0;
   rc.o = -1;
@@ -83,49 +74,99 @@ __device__ __forceinline__ RowCtx row_of(const DevPlan& p, const ReqInfo& ri, in
   return rc;
 }
 
-__global__ void __launch_bounds__(256)
-mark_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
-            int64_t lse_split_stride) {
-  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= p.mark_warps) return;
-  int w, g;
-  const int b = find_word(p, wid, &w, &g);
-  if (b < 0) return;
-  const ReqInfo ri = p.reqs[b];
-  const RowCtx rc = row_of(p, ri, g, w, lane);
-  for (int s = 0; s < p.K; ++s) {
-    int pg = rc.valid ? __ldg(idx + rc.r * p.K + s) : -1;
-    if (rc.valid && pg < 0) lse[s * lse_split_stride + rc.r] = -INFINITY;
-    if (rc.valid && pg > rc.o) {
-      set_status(p.status, DEV_BAD_INDEX);
-      pg = -1;
+// The selections of one row, held by its thread.  KV > 0: the first K of KV register slots
+// (K a multiple of 4, read as 16-byte vectors, the rest -1); KV == 0: read from global memory
+// at each use (any K).
+template <int KV>
+struct RowSel {
+  int v[KV > 0 ? KV : 1];
+  const int32_t* row;
+  int K;
+  __device__ __forceinline__ void load(const int32_t* idx, const RowCtx& rc, int k) {
+    K = k;
+    row = idx + rc.r * k;
+    if (KV > 0) {
+#pragma unroll
+      for (int q = 0; q < KV / 4; ++q) {
+        int4 x = make_int4(-1, -1, -1, -1);
+        if (rc.valid && 4 * q < k) x = __ldg(reinterpret_cast<const int4*>(row) + q);
+        v[4 * q] = x.x;
+        v[4 * q + 1] = x.y;
+        v[4 * q + 2] = x.z;
+        v[4 * q + 3] = x.w;
+      }
     }
-    // unique negative keys for inactive lanes so they only match themselves
-    const int key = pg >= 0 ? pg : -1 - lane;
-    const uint32_t mask = __match_any_sync(0xffffffffu, key);
-    if (pg >= 0 && lane == __ffs(mask) - 1)
-      atomicOr(p.bitmap + ri.bm_base + (int64_t)(pg * p.Hkv + g) * ri.bm_words + w, mask);
   }
+  __device__ __forceinline__ int n() const { return KV > 0 ? KV : K; }
+  __device__ __forceinline__ int get(int s) const { return KV > 0 ? v[s] : __ldg(row + s); }
+};
+
+// The row's valid selections in pages [p0, p0 + 64) as a bit mask (bit d: page p0 + d).
+template <int KV>
+__device__ __forceinline__ uint64_t row_mask(const RowSel<KV>& sel, const RowCtx& rc, int p0) {
+  uint64_t m = 0;
+  if (rc.valid) {
+#pragma unroll
+    for (int s = 0; s < sel.n(); ++s) {
+      const int pg = sel.get(s);
+      const int d = pg - p0;
+      if (d >= 0 && d < kInvPages && pg <= rc.o) m |= 1ull << d;
+    }
+  }
+  return m;
 }
 
-__global__ void __launch_bounds__(256) count_kernel(DevPlan p) {
-  __shared__ int sh[8];
-  int bucket, pg, g, c;
-  const int b = find_chunk(p, blockIdx.x, &bucket, &pg, &g, &c);
-  if (b < 0) return;
+// Turns the warp's 32 row masks around into one 32-row mask per page: tm[d][warp] bit l set
+// when row l of the warp selected page p0 + d.
+__device__ __forceinline__ void masks_to_smem(uint32_t (*tm)[kChunkWords + 1], uint64_t m, int warp,
+                                              int lane) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t b0 = __ballot_sync(0xffffffffu, (uint32_t)(m >> j) & 1u);
+    const uint32_t b1 = __ballot_sync(0xffffffffu, (uint32_t)(m >> (j + 32)) & 1u);
+    if (lane == j) {
+      lo = b0;
+      hi = b1;
+    }
+  }
+  tm[lane][warp] = lo;
+  tm[lane + 32][warp] = hi;
+}
+
+template <int KV>
+__global__ void __launch_bounds__(256)
+count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
+             int64_t lse_split_stride) {
+  __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
+  int g, c;
+  const int b = find_block(p, blockIdx.x, &g, &c);
+  if (b < 0) return;  // uniform over the block
   const ReqInfo ri = p.reqs[b];
-  const uint32_t* words = p.bitmap + ri.bm_base + (int64_t)(pg * p.Hkv + g) * ri.bm_words;
-  const int w0 = c * kChunkWords, w1 = min(ri.bm_words, w0 + kChunkWords);
-  int n = 0;
-  for (int w = w0 + threadIdx.x; w < w1; w += blockDim.x) n += __popc(words[w]);
-  n = __reduce_add_sync(0xffffffffu, n);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = n;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int t = 0;
-    for (int i = 0; i < 8; ++i) t += sh[i];
-    p.chunk_offsets[blockIdx.x] = t;  // a count here; the scan turns it into an offset
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
+  RowSel<KV> sel;
+  sel.load(idx, rc, p.K);
+  if (rc.valid) {
+#pragma unroll
+    for (int s = 0; s < sel.n(); ++s) {
+      if (s >= p.K) break;
+      const int pg = sel.get(s);
+      if (pg < 0) lse[s * lse_split_stride + rc.r] = -INFINITY;
+      else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
+    }
+  }
+  for (int p0 = 0; p0 < ri.npages; p0 += kInvPages) {
+    masks_to_smem(tm, row_mask(sel, rc, p0), warp, lane);
+    __syncthreads();
+    const int d = threadIdx.x;
+    if (d < kInvPages && p0 + d < ri.npages) {
+      int n = 0;
+#pragma unroll 8
+      for (int v = 0; v < kChunkWords; ++v) n += __popc(tm[d][v]);
+      p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)] = n;  // a count until step 2
+    }
+    __syncthreads();
   }
 }
 
@@ -156,116 +197,115 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* out, int* sh) {
   return total;
 }
 
-// First chunk of bucket `bucket` (buckets are laid out request by request, page-major).
-__device__ __forceinline__ int first_chunk(const DevPlan& p, int bucket) {
-  const int gp = bucket / p.Hkv, g = bucket % p.Hkv;
-  const ReqInfo& ri = p.reqs[p.page_req[gp]];
-  return ri.ch_base + ((gp - ri.page_base) * p.Hkv + g) * ri.ch_per_bucket;
-}
-
-__global__ void __launch_bounds__(1024) scan_kernel(DevPlan p) {
-  __shared__ int sh[32];
-  const int nc = p.num_chunks;
-  {  // chunk counts -> exclusive offsets (in place)
-    const int per = (nc + 1023) / 1024;
-    const int c0 = threadIdx.x * per;
-    int cnt = 0;
-    for (int c = c0; c < c0 + per && c < nc; ++c) cnt += p.chunk_offsets[c];
-    int off;
-    const int total = block_exclusive_scan(cnt, &off, sh);
-    for (int c = c0; c < c0 + per && c < nc; ++c) {
-      const int x = p.chunk_offsets[c];
-      p.chunk_offsets[c] = off;
-      off += x;
-    }
-    if (threadIdx.x == 0) {
-      p.chunk_offsets[nc] = total;
-      if (total > p.max_entries) set_status(p.status, DEV_OVERFLOW);
-    }
-  }
-  __syncthreads();
-  // bucket offsets and the forward work list
-  const int nb = p.num_buckets;
-  const int per = (nb + 1023) / 1024;
-  const int b0 = threadIdx.x * per;
+// Step 3 (one block): bucket totals -> CSR offsets (in place), then the forward's work list.
+// The totals were written by other blocks of this grid, so they are read past L1.
+__device__ __forceinline__ void scan_buckets(const DevPlan& p, int* sh) {
+  const int nb = p.num_buckets, nt = blockDim.x;
+  const int per = (nb + nt - 1) / nt;
+  const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
   const int per_task = kFwdTaskGroups * 128;
-  int ntask = 0;
-  for (int b = b0; b < b0 + per && b < nb; ++b) {
-    const int beg = p.chunk_offsets[first_chunk(p, b)];
-    const int end = b + 1 < nb ? p.chunk_offsets[first_chunk(p, b + 1)] : p.chunk_offsets[nc];
-    ntask += (end - beg + per_task - 1) / per_task;
+  int cnt = 0, ntask = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int t = __ldcg(p.bucket_offsets + b);
+    cnt += t;
+    ntask += (t + per_task - 1) / per_task;
   }
-  int toff;
+  int off, toff;
+  const int total = block_exclusive_scan(cnt, &off, sh);
   const int ttotal = block_exclusive_scan(ntask, &toff, sh);
-  for (int b = b0; b < b0 + per && b < nb; ++b) {
-    const int beg = p.chunk_offsets[first_chunk(p, b)];
-    const int end = b + 1 < nb ? p.chunk_offsets[first_chunk(p, b + 1)] : p.chunk_offsets[nc];
-    p.bucket_offsets[b] = beg;
-    for (int e = beg; e < end; e += per_task) {
+  for (int b = b0; b < b1; ++b) {
+    const int t = __ldcg(p.bucket_offsets + b);
+    p.bucket_offsets[b] = off;
+    for (int e = off; e < off + t; e += per_task) {
       if (toff < p.max_fwd_tasks) {
-        FwdTask t;
-        t.bucket = b;
-        t.entry_begin = e;
-        t.count = min(per_task, end - e);
-        t.pad = 0;
-        p.fwd_tasks[toff] = t;
+        FwdTask ft;
+        ft.bucket = b;
+        ft.entry_begin = e;
+        ft.count = min(per_task, off + t - e);
+        ft.pad = 0;
+        p.fwd_tasks[toff] = ft;
       }
       ++toff;
     }
+    off += t;
   }
   if (threadIdx.x == 0) {
-    p.bucket_offsets[nb] = p.chunk_offsets[nc];
+    p.bucket_offsets[nb] = total;
+    if (total > p.max_entries) set_status(p.status, DEV_OVERFLOW);
     p.counters[2] = min(ttotal, p.max_fwd_tasks);
     if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
   }
 }
 
-__global__ void __launch_bounds__(256) prefix_kernel(DevPlan p) {
+// Step 2: a block per bucket turns its chunk counts into bucket-local exclusive offsets and
+// leaves the bucket's total in bucket_offsets[bucket]; the last block to finish runs step 3.
+__global__ void __launch_bounds__(256) scan_kernel(DevPlan p) {
   __shared__ int sh[32];
-  constexpr int WPT = kChunkWords / 256;  // words per thread
-  int bucket, pg, g, c;
-  const int b = find_chunk(p, blockIdx.x, &bucket, &pg, &g, &c);
-  if (b < 0) return;
-  const ReqInfo ri = p.reqs[b];
-  const int64_t wbase = ri.bm_base + (int64_t)(pg * p.Hkv + g) * ri.bm_words;
-  const int w0 = c * kChunkWords + threadIdx.x * WPT;
-  int n = 0;
-  uint32_t bits[WPT];
-#pragma unroll
-  for (int i = 0; i < WPT; ++i) {
-    const int w = w0 + i;
-    bits[i] = w < ri.bm_words ? p.bitmap[wbase + w] : 0u;
-    n += __popc(bits[i]);
-  }
+  __shared__ int last;
+  const int bk = blockIdx.x;
+  const int gp = bk / p.Hkv, g = bk % p.Hkv;
+  const ReqInfo ri = p.reqs[p.page_req[gp]];
+  int32_t* cnt = p.chunk_offsets + chunk_id(p, ri, gp - ri.page_base, g, 0);
+  const int n = ri.ch_per_bucket;
+  const int per = (n + 255) / 256;
+  const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+  int x = 0;
+  for (int i = i0; i < i1; ++i) x += cnt[i];
   int off;
-  block_exclusive_scan(n, &off, sh);
-  off += p.chunk_offsets[blockIdx.x];
-#pragma unroll
-  for (int i = 0; i < WPT; ++i) {
-    const int w = w0 + i;
-    if (w < ri.bm_words) p.word_pos[wbase + w] = off;
-    off += __popc(bits[i]);
+  const int total = block_exclusive_scan(x, &off, sh);
+  for (int i = i0; i < i1; ++i) {
+    const int v = cnt[i];
+    cnt[i] = off;
+    off += v;
   }
+  if (threadIdx.x == 0) p.bucket_offsets[bk] = total;
+  __threadfence();  // this block's results are visible before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(p.counters + 3, 1) == p.num_buckets - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  scan_buckets(p, sh);
 }
 
+template <int KV>
 __global__ void __launch_bounds__(256)
 emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
-  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= p.mark_warps) return;
-  int w, g;
-  const int b = find_word(p, wid, &w, &g);
-  if (b < 0) return;
+  __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
+  __shared__ int pos0[kInvPages][kChunkWords + 1];  // first entry of (page, warp)
+  int g, c;
+  const int b = find_block(p, blockIdx.x, &g, &c);
+  if (b < 0) return;  // uniform over the block
   const ReqInfo ri = p.reqs[b];
-  const RowCtx rc = row_of(p, ri, g, w, lane);
-  if (!rc.valid) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
+  RowSel<KV> sel;
+  sel.load(idx, rc, p.K);
   const uint32_t below = (1u << lane) - 1u;
-  for (int s = 0; s < p.K; ++s) {
-    const int pg = __ldg(idx + rc.r * p.K + s);
-    if (pg < 0 || pg > rc.o) continue;
-    const int64_t wi = ri.bm_base + (int64_t)(pg * p.Hkv + g) * ri.bm_words + w;
-    const int pos = p.word_pos[wi] + __popc(p.bitmap[wi] & below);
-    p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
+  for (int p0 = 0; p0 < ri.npages; p0 += kInvPages) {
+    masks_to_smem(tm, row_mask(sel, rc, p0), warp, lane);
+    __syncthreads();
+    const int d = threadIdx.x;
+    if (d < kInvPages && p0 + d < ri.npages) {
+      const int bk = (ri.page_base + p0 + d) * p.Hkv + g;
+      int acc = p.bucket_offsets[bk] + p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)];
+      for (int v = 0; v < kChunkWords; ++v) {
+        pos0[d][v] = acc;
+        acc += __popc(tm[d][v]);
+      }
+    }
+    __syncthreads();
+    if (rc.valid) {
+#pragma unroll
+      for (int s = 0; s < sel.n(); ++s) {
+        const int pg = sel.get(s);
+        const int dd = pg - p0;
+        if (dd < 0 || dd >= kInvPages || pg > rc.o) continue;
+        const int pos = pos0[dd][warp] + __popc(tm[dd][warp] & below);
+        p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -274,25 +314,20 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
 cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
                              int64_t lse_split_stride, cudaStream_t st) {
   cudaError_t e;
-  e = cudaMemsetAsync(p.bitmap, 0, sizeof(uint32_t) * (size_t)p.bm_total_words, st);
-  if (e != cudaSuccess) return e;
-  const unsigned wgrid = (unsigned)((p.mark_warps + 7) / 8);
-  if (wgrid > 0) {
-    mark_kernel<<<wgrid, 256, 0, st>>>(p, idx, lse, lse_split_stride);
+  // selections held in registers when top_k is a multiple of 4 up to 16
+  const int kv = (p.K % 4 == 0 && p.K <= 16) ? 16 : 0;
+  const unsigned nblk = (unsigned)p.inv_blocks;
+  if (nblk > 0) {
+    if (kv == 16) count_kernel<16><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);
+    else count_kernel<0><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (p.num_chunks > 0) {
-    count_kernel<<<(unsigned)p.num_chunks, 256, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  scan_kernel<<<1, 1024, 0, st>>>(p);
+  // counters[3] (buckets scanned) was zeroed with the forward's task counters
+  scan_kernel<<<(unsigned)p.num_buckets, 256, 0, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.num_chunks > 0) {
-    prefix_kernel<<<(unsigned)p.num_chunks, 256, 0, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (wgrid > 0) {
-    emit_kernel<<<wgrid, 256, 0, st>>>(p, idx);
+  if (nblk > 0) {
+    if (kv == 16) emit_kernel<16><<<nblk, 256, 0, st>>>(p, idx);
+    else emit_kernel<0><<<nblk, 256, 0, st>>>(p, idx);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -10,7 +10,8 @@ namespace sps {
 constexpr int kPage = 128;         // tokens per KV page
 constexpr int kMaxTopK = 64;
 constexpr int kFwdTaskGroups = 8;  // 128-row query groups per forward work item
-constexpr int kChunkWords = 2048;  // bitmap words per prefix-scan chunk (256 threads x 8)
+constexpr int kChunkWords = 8;     // 32-row words per inversion chunk (one 256-thread block)
+constexpr int kInvPages = 64;      // pages per inversion window (one 64-bit row mask)
 
 // One request of the batch, as the kernels see it.
 struct ReqInfo {
@@ -19,10 +20,10 @@ struct ReqInfo {
   int32_t ctx;        // cached tokens before them
   int32_t npages;     // visible pages of the request's last token (own page + 1)
   int32_t page_base;  // running sum of npages over earlier requests
-  int32_t bm_base;    // first selection-bitmap word of the request
-  int32_t bm_words;   // words per (page, KV head) bucket: ceil(q_len * H/H_kv / 32)
-  int32_t ch_base;    // first bitmap chunk of the request
-  int32_t ch_per_bucket;  // chunks per bucket: ceil(bm_words / kChunkWords)
+  int32_t blk_base;   // first inversion block of the request (blocks: KV head x chunk)
+  int32_t words;      // 32-row words of one KV group's rows: ceil(q_len * H/H_kv / 32)
+  int32_t ch_base;    // first inversion chunk of the request
+  int32_t ch_per_bucket;  // chunks per (page, KV head) bucket: ceil(words / kChunkWords)
   int32_t pad[5];
 };
 
@@ -42,20 +43,19 @@ struct FwdTask {
 // Everything a kernel needs about the plan, passed by value.
 struct DevPlan {
   int32_t batch, T, H, Hkv, Hg, D, K, max_pages, num_phys;
-  int32_t num_buckets, max_entries, max_fwd_tasks, n_idx_tasks, total_pages, bm_total_words;
-  int64_t mark_warps;       // sum over requests of H_kv * bm_words (one warp per bitmap word)
+  int32_t num_buckets, max_entries, max_fwd_tasks, n_idx_tasks, total_pages;
+  int32_t inv_blocks;       // sum over requests of H_kv * ch_per_bucket
   float sm_scale;
   int32_t* status;
-  int32_t* counters;        // [0] indexer task cursor, [1] forward task cursor, [2] fwd task count
+  int32_t* counters;        // [0] indexer task cursor, [1] forward task cursor, [2] fwd task
+                            // count, [3] inversion buckets scanned
   const int32_t* tok_pos;   // [T]
   const int32_t* tok_req;   // [T]
   const ReqInfo* reqs;      // [batch]
   const int32_t* page_req;  // [total_pages]: request of each global page slot
   const IdxTask* idx_tasks; // [n_idx_tasks]
-  uint32_t* bitmap;         // [bm_total_words]
-  int32_t num_chunks;       // bitmap chunks (buckets x chunks per bucket)
+  int32_t num_chunks;       // inversion chunks (buckets x chunks per bucket)
   int32_t* chunk_offsets;   // [num_chunks + 1]: entries before each chunk
-  int32_t* word_pos;        // [bm_total_words]: entries before each bitmap word
   int32_t* bucket_offsets;  // [num_buckets + 1]
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
