@@ -11,6 +11,8 @@
 // (redux.sync) of the lanes' head keys and one ballot: the lowest lane whose head holds the
 // maximum has the winning page (ties go to the lower page) and shifts its next candidate up.
 // After n_sel - 1 rounds a ballot/popc prefix writes the chosen pages in ascending order.
+// Rows of more than 128 pages first filter their keys down to at most 64 candidates (see
+// topk_filter_kernel) and run the rounds on those.
 #include "ptx.cuh"
 #include "sps_internal.h"
 
@@ -100,6 +102,135 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
     if ((taken >> j) & 1u) out[before++] = base + j;
 }
 
+// Long rows (E >= 8 pages per lane): a filter first.  The (k-1)-th largest of the 32 lane
+// maxima, t0, taken one lane per round, is at most the row's (k-1)-th largest key (those k-1
+// maxima are k-1 distinct keys >= t0), so every page of the answer has key >= t0.  The keys
+// >= t0 are compacted in page order into two per lane (shared memory, at most 64 of them) and
+// the rounds above run on those; the row's own page, its last visible page, goes last.  A row
+// with more than 64 such keys (heavy ties) runs the rounds on all its keys instead.
+template <int E>
+__global__ void __launch_bounds__(256)
+topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
+                   int32_t* __restrict__ idx) {
+  __shared__ uint2 cand[8][64];  // per warp: (key, page) of the compacted candidates
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t r = (int64_t)blockIdx.x * 8 + warp;
+  const int64_t R = (int64_t)p.T * p.H;
+  if (r >= R) return;
+  const int o = __ldg(p.tok_pos + r / p.H) >> 7;
+  const int n = o + 1, K = p.K;
+  int32_t* out = idx + r * K;
+  if (n <= K) {  // every visible page is kept
+    for (int s = lane; s < K; s += 32) out[s] = s < n ? s : -1;
+    return;
+  }
+  const float* row = scores + r * pitch;
+  const int base = lane * E;
+  uint32_t key[E];
+  uint32_t lm = 0;  // the lane's largest key
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int page = base + j;
+    key[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
+    lm = max(lm, key[j]);
+  }
+  // t0: the (K-1)-th largest lane maximum (0 when fewer lanes hold candidates)
+  uint32_t t0 = 0, v = lm;
+  for (int round = 1; round < K; ++round) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, v);
+    t0 = m;
+    if (m == 0u) break;
+    const uint32_t tie = __ballot_sync(0xffffffffu, v == m);
+    if (lane == __ffs(tie) - 1) v = 0u;
+  }
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < E; ++j) cnt += (key[j] != 0u && key[j] >= t0) ? 1 : 0;
+  const int total = __reduce_add_sync(0xffffffffu, cnt);
+  const uint32_t lt = (1u << lane) - 1u;
+  if (total <= 64) {
+    int pos = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, pos, d);
+      if (lane >= d) pos += y;
+    }
+    pos -= cnt;
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      if (key[j] != 0u && key[j] >= t0) cand[warp][pos++] = make_uint2(key[j], (uint32_t)(base + j));
+    __syncwarp();
+    uint32_t ck[2], cp[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = 2 * lane + j;
+      ck[j] = i < total ? cand[warp][i].x : 0u;
+      cp[j] = (uint32_t)j;
+    }
+    const uint32_t page0 = 2 * lane < total ? cand[warp][2 * lane].y : 0u;
+    const uint32_t page1 = 2 * lane + 1 < total ? cand[warp][2 * lane + 1].y : 0u;
+    sort_best_first<2>(ck, cp);
+    int c = 0;
+#pragma unroll 4
+    for (int round = 1; round < K; ++round) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, ck[0]);
+      const uint32_t tie = __ballot_sync(0xffffffffu, ck[0] == m);
+      if (ck[0] == m && (tie & lt) == 0) {
+        ++c;
+        ck[0] = ck[1];
+        ck[1] = 0u;
+      }
+    }
+    uint32_t taken = 0;  // bit j: compacted candidate 2 lane + j selected
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (j < c) taken |= 1u << cp[j];
+    int before = __popc(taken);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, before, d);
+      if (lane >= d) before += y;
+    }
+    before -= __popc(taken);
+    if (taken & 1u) out[before++] = (int32_t)page0;
+    if (taken & 2u) out[before++] = (int32_t)page1;
+    if (lane == 0) out[K - 1] = o;  // the own page is the row's last visible page
+    return;
+  }
+  // heavy ties: the rounds on every key of the row
+  uint32_t pg[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) pg[j] = (uint32_t)j;
+  sort_best_first<E>(key, pg);
+  int c = 0;
+#pragma unroll 4
+  for (int round = 1; round < K; ++round) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t tie = __ballot_sync(0xffffffffu, key[0] == m);
+    if (key[0] == m && (tie & lt) == 0) {
+      ++c;
+#pragma unroll
+      for (int j = 0; j + 1 < E; ++j) key[j] = key[j + 1];
+      key[E - 1] = 0u;
+    }
+  }
+  uint32_t taken = 0;
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if (j < c) taken |= 1u << pg[j];
+  if (o / E == lane) taken |= 1u << (o % E);
+  int before = __popc(taken);
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, before, d);
+    if (lane >= d) before += y;
+  }
+  before -= __popc(taken);
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if ((taken >> j) & 1u) out[before++] = base + j;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, int32_t* idx,
@@ -110,8 +241,8 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
   if (p.max_pages <= 32) topk_kernel<1><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   else if (p.max_pages <= 64) topk_kernel<2><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   else if (p.max_pages <= 128) topk_kernel<4><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else if (p.max_pages <= 256) topk_kernel<8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else topk_kernel<16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  else if (p.max_pages <= 256) topk_filter_kernel<8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  else topk_filter_kernel<16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   return cudaGetLastError();
 }
 
