@@ -1,6 +1,6 @@
 // host.cpp -- C ABI of libsps: problem validation, the plan (per-token metadata, indexer work
-// list, workspace layout), the metadata upload, and the argument checks in front of every
-// kernel launch.  No device memory is ever allocated here.
+// list, workspace layout), the metadata upload (through a page-locked staging ring), and the
+// argument checks in front of every kernel launch.  No device memory is ever allocated here.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -40,6 +40,76 @@ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
+
+// Page-locked staging for the plan-metadata uploads, so that the host->device copy is a
+// plain asynchronous DMA on the caller's stream (a copy from pageable memory makes the GPU
+// wait while the driver stages it).  One ring per process, allocated on first use and never
+// freed; a region is reused only after the event recorded behind its copy has completed.
+// Uploads that do not fit, uploads into a stream being captured into a graph (the graph must
+// keep reading the plan's own copy), or a failed page-locking copy from pageable memory
+// instead.
+class StagingRing {
+ public:
+  cudaError_t upload(void* dst, const void* src, size_t n, cudaStream_t s) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+      (void)cudaGetLastError();
+      return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s);
+    }
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!buf_ && !failed_) {
+      if (cudaHostAlloc(reinterpret_cast<void**>(&buf_), kBytes, cudaHostAllocPortable) !=
+          cudaSuccess) {
+        buf_ = nullptr;
+        failed_ = true;
+        (void)cudaGetLastError();
+      }
+    }
+    if (!buf_ || n > kBytes / 2) return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s);
+    size_t off = head_;
+    if (off + n > kBytes) off = 0;
+    // wait for the copies still reading [off, off + n)
+    while (!live_.empty() && overlaps(live_.front(), off, off + n)) {
+      cudaError_t e = cudaEventSynchronize(live_.front().ev);
+      free_ev_.push_back(live_.front().ev);
+      live_.erase(live_.begin());
+      if (e != cudaSuccess) return e;
+    }
+    memcpy(buf_ + off, src, n);
+    cudaError_t e = cudaMemcpyAsync(dst, buf_ + off, n, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t ev;
+    if (!free_ev_.empty()) {
+      ev = free_ev_.back();
+      free_ev_.pop_back();
+    } else if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
+      return cudaStreamSynchronize(s);  // no event: the region is safe once the copy is done
+    }
+    if ((e = cudaEventRecord(ev, s)) != cudaSuccess) {
+      cudaEventDestroy(ev);
+      return cudaStreamSynchronize(s);
+    }
+    live_.push_back({off, off + n, ev});
+    head_ = (size_t)align_up((int64_t)(off + n), 256);
+    return cudaSuccess;
+  }
+
+ private:
+  struct Live {
+    size_t begin, end;
+    cudaEvent_t ev;
+  };
+  static bool overlaps(const Live& l, size_t b, size_t e) { return l.begin < e && b < l.end; }
+  static constexpr size_t kBytes = 16u << 20;
+  std::mutex mu_;
+  uint8_t* buf_ = nullptr;
+  bool failed_ = false;
+  size_t head_ = 0;
+  std::vector<Live> live_;  // in ring order
+  std::vector<cudaEvent_t> free_ev_;
+};
+
+StagingRing g_staging;
 
 }  // namespace
 
@@ -345,9 +415,8 @@ sps_status sps_plan_upload(const sps_plan* pl, void* ws, size_t ws_bytes, sps_st
   uint8_t* base = static_cast<uint8_t*>(ws);
   cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);  // status + counters
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
-  e = cudaMemcpyAsync(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes,
-                      cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan upload)");
+  e = g_staging.upload(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   return SPS_OK;
 }
 
@@ -721,8 +790,7 @@ sps_status sps_internal_fwd_noalloc(const sps_plan* pl, const void* q, float q_s
   // write this plan's metadata over the old one
   cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch header)");
-  e = cudaMemcpyAsync(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes,
-                      cudaMemcpyHostToDevice, s);
+  e = g_staging.upload(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan metadata -> scratch)");
   DevPlan d = make_dev_plan(pl, scratch);
   if (dev_status) d.status = dev_status;

@@ -11,7 +11,11 @@
 //   * warp 1 (MMA issuer, one thread): S_h = Q_h K^T, M = 128 rows, N = 128 keys, FP32
 //     accumulators in TMEM, double-buffered per head (4 x 128 columns).  The two heads' K
 //     steps are issued interleaved from descriptors built once per tile: a single thread has
-//     to issue an MMA every ~64 cycles to keep the tensor core busy, so the loop stays short;
+//     to issue an MMA every ~64 cycles to keep the tensor core busy, so the loop stays short.
+//     Each barrier wait in that thread stalls the MMA stream (~100 cycles), so a page step
+//     has one wait and one commit: the K ring's "full" barrier also collects the epilogue's
+//     release of the accumulator pair the step writes, and its "empty" barrier (the step's
+//     MMAs are done) is what the epilogue waits on;
 //   * warps 2-9 (epilogue, one warpgroup per head, a thread per row): the per-page row max
 //     comes straight out of TMEM with tcgen05.ld.red.max; only rows whose own page it is take
 //     the element-wise masked path (a warp-uniform vote picks the path).
@@ -35,8 +39,11 @@ struct IdxSmem {
   uint8_t q[kQStages][2][TILE];
   uint8_t k[kKStages][TILE];
   uint64_t q_full[kQStages], q_empty[kQStages];
+  // k_full[s]: the K tile of the stage's next page step has landed AND the accumulator pair
+  // that step writes has been read out (arrivals: the producer's expect_tx + one per epilogue
+  // warp); k_empty[s]: the step's MMAs are done (the K tile is free and its accumulators hold
+  // the scores)
   uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t acc_full[2], acc_empty[2];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
@@ -64,12 +71,8 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
     }
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(smem_u32(&sm.k_full[i]), 1);
+      mbar_init(smem_u32(&sm.k_full[i]), 1 + 8);
       mbar_init(smem_u32(&sm.k_empty[i]), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sm.acc_full[i]), 1);
-      mbar_init(smem_u32(&sm.acc_empty[i]), 8);  // one arrive per epilogue warp
     }
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort_flag = 0;
@@ -137,8 +140,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int pg = t.page_begin; pg < t.page_end; ++pg) {
           const int ks = k_it % kKStages;
           const int ab = a_it & 1;
-          if (!mbar_wait(smem_u32(&sm.k_full[ks]), (k_it / kKStages) & 1, abort_flag, status) ||
-              !mbar_wait(smem_u32(&sm.acc_empty[ab]), ((a_it >> 1) & 1) ^ 1, abort_flag, status)) {
+          if (!mbar_wait(smem_u32(&sm.k_full[ks]), (k_it / kKStages) & 1, abort_flag, status)) {
             ok = false;
             break;
           }
@@ -167,7 +169,6 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
           }
           mma_commit(smem_u32(&sm.k_empty[ks]));
-          mma_commit(smem_u32(&sm.acc_full[ab]));
           ++k_it;
           ++a_it;
         }
@@ -186,6 +187,11 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int row = quarter * 32 + lane;   // tile row = token within the tile
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     uint32_t a_it = 0;
+    // both accumulator pairs start free: page steps 0 and 1
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&sm.k_full[0]));
+      mbar_arrive(smem_u32(&sm.k_full[1]));
+    }
     for (int ti = blockIdx.x; ti < p.n_idx_tasks; ti += gridDim.x) {
       const IdxTask t = p.idx_tasks[ti];
       const ReqInfo ri = p.reqs[t.req];
@@ -196,7 +202,8 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       bool ok = true;
       for (int pg = t.page_begin; pg < t.page_end; ++pg) {
         const int ab = a_it & 1;
-        if (!mbar_wait(smem_u32(&sm.acc_full[ab]), (a_it >> 1) & 1, abort_flag, status)) {
+        if (!mbar_wait(smem_u32(&sm.k_empty[a_it % kKStages]), (a_it / kKStages) & 1, abort_flag,
+                       status)) {
           ok = false;
           break;
         }
@@ -229,7 +236,8 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[ab]));
+        // this accumulator pair is free for page step a_it + 2
+        if (lane == 0) mbar_arrive(smem_u32(&sm.k_full[(a_it + 2) % kKStages]));
         ++a_it;
       }
       if (!ok) break;
