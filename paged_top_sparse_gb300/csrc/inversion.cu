@@ -74,14 +74,20 @@ __device__ __forceinline__ RowCtx row_of(const DevPlan& p, const ReqInfo& ri, in
   return rc;
 }
 
-// The selections of one row, held by its thread.  KV > 0: the first K of KV register slots
-// (K a multiple of 4, read as 16-byte vectors, the rest -1); KV == 0: read from global memory
-// at each use (any K).
+// The selections of one row, held by its thread.  KV > 0: the first K of KV slots (K a
+// multiple of 4, read as 16-byte vectors, the rest -1), two 16-bit values per register; a
+// value outside [-1, 32767] is stored as -1 (negative: empty) or 32767 (past every own page:
+// invalid), which keeps its meaning.  KV == 0: read from global memory at each use (any K).
 template <int KV>
 struct RowSel {
-  int v[KV > 0 ? KV : 1];
+  uint32_t v[KV > 0 ? KV / 2 : 1];
   const int32_t* row;
   int K;
+  static __device__ __forceinline__ uint32_t pack(int a, int b) {
+    a = min(max(a, -1), 32767);
+    b = min(max(b, -1), 32767);
+    return ((uint32_t)a & 0xffffu) | ((uint32_t)b << 16);
+  }
   __device__ __forceinline__ void load(const int32_t* idx, const RowCtx& rc, int k) {
     K = k;
     row = idx + rc.r * k;
@@ -90,15 +96,16 @@ struct RowSel {
       for (int q = 0; q < KV / 4; ++q) {
         int4 x = make_int4(-1, -1, -1, -1);
         if (rc.valid && 4 * q < k) x = __ldg(reinterpret_cast<const int4*>(row) + q);
-        v[4 * q] = x.x;
-        v[4 * q + 1] = x.y;
-        v[4 * q + 2] = x.z;
-        v[4 * q + 3] = x.w;
+        v[2 * q] = pack(x.x, x.y);
+        v[2 * q + 1] = pack(x.z, x.w);
       }
     }
   }
   __device__ __forceinline__ int n() const { return KV > 0 ? KV : K; }
-  __device__ __forceinline__ int get(int s) const { return KV > 0 ? v[s] : __ldg(row + s); }
+  __device__ __forceinline__ int get(int s) const {
+    if (KV > 0) return (int)(int16_t)(v[s >> 1] >> (16 * (s & 1)));
+    return __ldg(row + s);
+  }
 };
 
 // The row's valid selections in pages [p0, p0 + 64) as a bit mask (bit d: page p0 + d).
@@ -135,14 +142,14 @@ __device__ __forceinline__ void masks_to_smem(uint32_t (*tm)[kChunkWords + 1], u
 }
 
 template <int KV>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 8)
 count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
              int64_t lse_split_stride) {
   __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
   int g, c;
   const int b = find_block(p, blockIdx.x, &g, &c);
   if (b < 0) return;  // uniform over the block
-  const ReqInfo ri = p.reqs[b];
+  const ReqInfo& ri = p.reqs[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
   RowSel<KV> sel;
@@ -269,14 +276,14 @@ __global__ void __launch_bounds__(256) scan_kernel(DevPlan p) {
 }
 
 template <int KV>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 8)
 emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
   __shared__ int pos0[kInvPages][kChunkWords + 1];  // first entry of (page, warp)
   int g, c;
   const int b = find_block(p, blockIdx.x, &g, &c);
   if (b < 0) return;  // uniform over the block
-  const ReqInfo ri = p.reqs[b];
+  const ReqInfo& ri = p.reqs[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
   RowSel<KV> sel;
