@@ -4,18 +4,19 @@
 //
 // Design (GB300, one CTA per SM, persistent over a host-built work list):
 //   * work item = query tile (up to 128 consecutive tokens of one request) x 1-2 query heads
-//     of one KV group x a chunk of pages;
+//     of one KV group x a chunk of pages, walked two pages at a time;
 //   * warp 0 (TMA producer): per item, the Q tile of each head (3-D tensor map over
-//     [T][H][D], 128-byte swizzle) into a 2-stage Q ring; per page, the physical K tile
-//     (looked up in the page table) into a 3-stage K ring;
-//   * warp 1 (MMA issuer, one thread): S_h = Q_h K^T, M = 128 rows, N = 128 keys, FP32
-//     accumulators in TMEM, double-buffered per head (4 x 128 columns).  The two heads' K
-//     steps are issued interleaved from descriptors built once per tile: a single thread has
-//     to issue an MMA every ~64 cycles to keep the tensor core busy, so the loop stays short.
-//     Each barrier wait in that thread stalls the MMA stream (~100 cycles), so a page step
-//     has one wait and one commit: the K ring's "full" barrier also collects the epilogue's
-//     release of the accumulator pair the step writes, and its "empty" barrier (the step's
-//     MMAs are done) is what the epilogue waits on;
+//     [T][H][D], 128-byte swizzle) into a ring of three one-head slots (the next item's first
+//     head loads while the current item runs); per page pair, the two physical K tiles
+//     (looked up in the page table) stacked into one 256-row operand, in a 2-stage ring;
+//   * warp 1 (MMA issuer, one thread): S_h = Q_h K^T with M = 128 rows and N = 256 keys (two
+//     pages per instruction), FP32 accumulators in TMEM, one 256-column buffer per head.  A
+//     128 x 128 x 16 MMA with both operands in shared memory reads 8 KB in 64 cycles, all of
+//     the SM's shared-memory bandwidth, and the K tiles land in the same memory; at N = 256
+//     one read of the Q operand serves two pages, which leaves room for the K loads.  Each
+//     barrier wait in this thread stalls the MMA stream, so a head step has one wait and one
+//     commit: the K ring's "full" barrier also collects the release of head 0's accumulator,
+//     and head 1's step waits only for its own accumulator;
 //   * warps 2-9 (epilogue, one warpgroup per head, a thread per row): the per-page row max
 //     comes straight out of TMEM with tcgen05.ld.red.max; only rows whose own page it is take
 //     the element-wise masked path (a warp-uniform vote picks the path).
@@ -29,21 +30,23 @@
 namespace sps {
 namespace {
 
-constexpr int kQStages = 2;
-constexpr int kKStages = 3;
+constexpr int kQSlots = 3;     // one-head Q tiles: an item's two heads + the next item's first
+constexpr int kKStages = 2;    // page pairs
 constexpr int kThreads = 320;  // 10 warps
 
 template <int ROWB>  // bytes per Q/K row: 128 or 256
 struct IdxSmem {
   static constexpr int TILE = 128 * ROWB;  // one 128-row tile
-  uint8_t q[kQStages][2][TILE];
-  uint8_t k[kKStages][TILE];
-  uint64_t q_full[kQStages], q_empty[kQStages];
-  // k_full[s]: the K tile of the stage's next page step has landed AND the accumulator pair
-  // that step writes has been read out (arrivals: the producer's expect_tx + one per epilogue
-  // warp); k_empty[s]: the step's MMAs are done (the K tile is free and its accumulators hold
-  // the scores)
-  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint8_t q[kQSlots][TILE];                // [column block][128 rows][128 B]
+  uint8_t k[kKStages][2 * TILE];           // [column block][256 rows][128 B], page A then B
+  uint64_t q_full[kQSlots], q_empty[kQSlots];
+  // k_full[s]: the stage's page pair has landed AND head 0's accumulator has been read out
+  // (arrivals: the producer's expect_tx + one per head-0 epilogue warp); a1_free[s]: head 1's
+  // accumulator has been read out for the stage's pair; k_empty[s]: both heads' MMAs of the
+  // pair are done (the K tiles are free, head 1's scores are in TMEM); a0_full: head 0's MMAs
+  // of the current pair are done
+  uint64_t k_full[kKStages], a1_free[kKStages], k_empty[kKStages];
+  uint64_t a0_full;
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
@@ -58,7 +61,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   constexpr int DB = ROWB / 128;       // 128-byte column blocks per row
   constexpr int KSTEPS = DB * 4;       // 32-byte K steps per row
   constexpr int TILE = Smem::TILE;
-  constexpr uint32_t IDESC = idesc_mma(BF16IN, BF16IN, 128, 128, false, false);
+  constexpr int CB = 128 * 128;        // bytes of one column block of a 128-row tile
+  constexpr uint32_t IDESC2 = idesc_mma(BF16IN, BF16IN, 128, 256, false, false);
+  constexpr uint32_t IDESC1 = idesc_mma(BF16IN, BF16IN, 128, 128, false, false);
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -66,14 +71,16 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   int32_t* status = p.status;
 
   if (tid == 0) {
-    for (int i = 0; i < kQStages; ++i) {
+    for (int i = 0; i < kQSlots; ++i) {
       mbar_init(smem_u32(&sm.q_full[i]), 1);
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
     }
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(smem_u32(&sm.k_full[i]), 1 + 8);
+      mbar_init(smem_u32(&sm.k_full[i]), 1 + 4);
+      mbar_init(smem_u32(&sm.a1_free[i]), 4);
       mbar_init(smem_u32(&sm.k_empty[i]), 1);
     }
+    mbar_init(smem_u32(&sm.a0_full), 1);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -85,7 +92,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  const uint32_t tmem = sm.tmem_base;  // head h's accumulator: columns 256 h .. 256 h + 255
   volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == 0) {
@@ -93,88 +100,116 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      uint32_t q_it = 0, k_it = 0;
-      for (int ti = blockIdx.x; ti < p.n_idx_tasks && !*abort_flag; ti += gridDim.x) {
+      uint32_t jp = 0, hs = 0;  // page pairs and Q head slots loaded so far
+      bool ok = true;
+      for (int ti = blockIdx.x; ti < p.n_idx_tasks && ok && !*abort_flag; ti += gridDim.x) {
         const IdxTask t = p.idx_tasks[ti];
-        const int qs = q_it % kQStages;
-        if (!mbar_wait(smem_u32(&sm.q_empty[qs]), ((q_it / kQStages) & 1) ^ 1, abort_flag, status))
-          break;
-        const uint32_t qf = smem_u32(&sm.q_full[qs]);
-        mbar_expect_tx(qf, t.nh * TILE);
-        for (int h = 0; h < t.nh; ++h)
-          for (int db = 0; db < DB; ++db)
-            tma_load_3d(smem_u32(sm.q[qs][h]) + db * 16384, &tmQ, db * (FP8 ? 128 : 64),
-                        t.h0 + h, t.tok0, qf);
-        ++q_it;
+        // Q of head 0 goes before the item's first page pair, Q of head 1 after it: head 1's
+        // slot may still hold the previous item's head 0
         const int32_t* pt_row = page_table + (int64_t)t.req * p.max_pages;
-        for (int pg = t.page_begin; pg < t.page_end; ++pg) {
-          const int ks = k_it % kKStages;
-          if (!mbar_wait(smem_u32(&sm.k_empty[ks]), ((k_it / kKStages) & 1) ^ 1, abort_flag,
-                         status))
-            break;
-          int phys = __ldg(pt_row + pg);
-          if (phys < 0 || phys >= p.num_phys) {
-            set_status(status, DEV_BAD_PAGE);
-            phys = 0;
+        for (int pb = t.page_begin; pb < t.page_end && ok; pb += 2, ++jp) {
+          if (pb == t.page_begin) {  // Q of head 0
+            const uint32_t s0 = hs % kQSlots;
+            if (!mbar_wait(smem_u32(&sm.q_empty[s0]), ((hs / kQSlots) & 1) ^ 1, abort_flag,
+                           status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t qf = smem_u32(&sm.q_full[s0]);
+            mbar_expect_tx(qf, TILE);
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(smem_u32(sm.q[s0]) + db * CB, &tmQ, db * (FP8 ? 128 : 64), t.h0,
+                          t.tok0, qf);
           }
+          const int ks = jp % kKStages;
+          if (!mbar_wait(smem_u32(&sm.k_empty[ks]), ((jp / kKStages) & 1) ^ 1, abort_flag,
+                         status)) {
+            ok = false;
+            break;
+          }
+          const int npg = min(2, t.page_end - pb);
           const uint32_t kf = smem_u32(&sm.k_full[ks]);
-          mbar_expect_tx(kf, TILE);
-          const int krow = (phys * p.Hkv + t.g) * 128;
-          for (int db = 0; db < DB; ++db)
-            tma_load_2d(smem_u32(sm.k[ks]) + db * 16384, &tmK, db * (FP8 ? 128 : 64), krow, kf);
-          ++k_it;
+          mbar_expect_tx(kf, npg * TILE);
+          for (int u = 0; u < npg; ++u) {
+            int phys = __ldg(pt_row + pb + u);
+            if (phys < 0 || phys >= p.num_phys) {
+              set_status(status, DEV_BAD_PAGE);
+              phys = 0;
+            }
+            const int krow = (phys * p.Hkv + t.g) * 128;
+            for (int db = 0; db < DB; ++db)
+              tma_load_2d(smem_u32(sm.k[ks]) + db * 2 * CB + u * CB, &tmK, db * (FP8 ? 128 : 64),
+                          krow, kf);
+          }
+          if (pb == t.page_begin && t.nh == 2) {  // Q of head 1, after the first pair
+            const uint32_t s1 = (hs + 1) % kQSlots;
+            if (!mbar_wait(smem_u32(&sm.q_empty[s1]), (((hs + 1) / kQSlots) & 1) ^ 1, abort_flag,
+                           status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t qf = smem_u32(&sm.q_full[s1]);
+            mbar_expect_tx(qf, TILE);
+            for (int db = 0; db < DB; ++db)
+              tma_load_3d(smem_u32(sm.q[s1]) + db * CB, &tmQ, db * (FP8 ? 128 : 64), t.h0 + 1,
+                          t.tok0, qf);
+          }
         }
+        hs += t.nh;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t q_it = 0, k_it = 0, a_it = 0;
-      for (int ti = blockIdx.x; ti < p.n_idx_tasks && !*abort_flag; ti += gridDim.x) {
+      uint32_t jp = 0, hs = 0;
+      bool ok = true;
+      for (int ti = blockIdx.x; ti < p.n_idx_tasks && ok && !*abort_flag; ti += gridDim.x) {
         const IdxTask t = p.idx_tasks[ti];
-        const int qs = q_it % kQStages;
-        if (!mbar_wait(smem_u32(&sm.q_full[qs]), (q_it / kQStages) & 1, abort_flag, status)) break;
-        bool ok = true;
-        const uint64_t ad0 = sdesc_sw128(smem_u32(sm.q[qs][0]), 16, 1024);
-        const uint64_t ad1 = sdesc_sw128(smem_u32(sm.q[qs][1]), 16, 1024);
-        for (int pg = t.page_begin; pg < t.page_end; ++pg) {
-          const int ks = k_it % kKStages;
-          const int ab = a_it & 1;
-          if (!mbar_wait(smem_u32(&sm.k_full[ks]), (k_it / kKStages) & 1, abort_flag, status)) {
+        const uint32_t s0 = hs % kQSlots, s1 = (hs + 1) % kQSlots;
+        if (!mbar_wait(smem_u32(&sm.q_full[s0]), (hs / kQSlots) & 1, abort_flag, status)) break;
+        // descriptors built once per item; a K step only moves the start address (16-byte units)
+        const uint64_t ad0 = sdesc_sw128(smem_u32(sm.q[s0]), 16, 1024);
+        const uint64_t ad1 = sdesc_sw128(smem_u32(sm.q[s1]), 16, 1024);
+        for (int pb = t.page_begin; pb < t.page_end; pb += 2, ++jp) {
+          const int ks = jp % kKStages;
+          const uint32_t ph = (jp / kKStages) & 1;
+          const uint32_t idesc = pb + 1 < t.page_end ? IDESC2 : IDESC1;
+          if (!mbar_wait(smem_u32(&sm.k_full[ks]), ph, abort_flag, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptors built once; a K step only moves the start address (16-byte units)
-          const uint64_t bd0 = sdesc_sw128(smem_u32(sm.k[ks]), 16, 1024);
-          const uint32_t d0 = tmem + (uint32_t)(ab * 256);
+          const uint64_t bd = sdesc_sw128(smem_u32(sm.k[ks]), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint64_t oa = (uint64_t)(((kk / 4) * CB + (kk % 4) * 32) >> 4);
+            const uint64_t ob = (uint64_t)(((kk / 4) * 2 * CB + (kk % 4) * 32) >> 4);
+            if (FP8) mma_f8_ss(tmem, ad0 + oa, bd + ob, idesc, kk > 0);
+            else mma_f16_ss(tmem, ad0 + oa, bd + ob, idesc, kk > 0);
+          }
+          mma_commit(smem_u32(&sm.a0_full));
           if (t.nh == 2) {
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-              const uint64_t off = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
-              if (FP8) {
-                mma_f8_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
-                mma_f8_ss(d0 + 128, ad1 + off, bd0 + off, IDESC, kk > 0);
-              } else {
-                mma_f16_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
-                mma_f16_ss(d0 + 128, ad1 + off, bd0 + off, IDESC, kk > 0);
-              }
+            if ((pb == t.page_begin &&
+                 !mbar_wait(smem_u32(&sm.q_full[s1]), ((hs + 1) / kQSlots) & 1, abort_flag,
+                            status)) ||
+                !mbar_wait(smem_u32(&sm.a1_free[ks]), ph, abort_flag, status)) {
+              ok = false;
+              break;
             }
-          } else {
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
-              const uint64_t off = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
-              if (FP8) mma_f8_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
-              else mma_f16_ss(d0, ad0 + off, bd0 + off, IDESC, kk > 0);
+              const uint64_t oa = (uint64_t)(((kk / 4) * CB + (kk % 4) * 32) >> 4);
+              const uint64_t ob = (uint64_t)(((kk / 4) * 2 * CB + (kk % 4) * 32) >> 4);
+              if (FP8) mma_f8_ss(tmem + 256, ad1 + oa, bd + ob, idesc, kk > 0);
+              else mma_f16_ss(tmem + 256, ad1 + oa, bd + ob, idesc, kk > 0);
             }
           }
           mma_commit(smem_u32(&sm.k_empty[ks]));
-          ++k_it;
-          ++a_it;
         }
-        mma_commit(smem_u32(&sm.q_empty[qs]));
-        ++q_it;
-        if (!ok) break;
+        mma_commit(smem_u32(&sm.q_empty[s0]));
+        if (t.nh == 2) mma_commit(smem_u32(&sm.q_empty[s1]));
+        hs += t.nh;
       }
       // every commit above has landed before the CTA may exit
       mma_commit(smem_u32(&sm.done));
@@ -182,16 +217,13 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------ epilogue: warps 2..9
-    const int e = (warp - 2) / 4;          // head of the pair
+    const int e = (warp - 2) / 4;          // head of the pair = accumulator
     const int quarter = warp % 4;          // TMEM lanes 32*quarter ...
     const int row = quarter * 32 + lane;   // tile row = token within the tile
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    uint32_t a_it = 0;
-    // both accumulator pairs start free: page steps 0 and 1
-    if (lane == 0) {
-      mbar_arrive(smem_u32(&sm.k_full[0]));
-      mbar_arrive(smem_u32(&sm.k_full[1]));
-    }
+    uint32_t jp = 0;
+    // both accumulators start free (page pair 0)
+    if (lane == 0) mbar_arrive(smem_u32(e == 0 ? &sm.k_full[0] : &sm.a1_free[0]));
     for (int ti = blockIdx.x; ti < p.n_idx_tasks; ti += gridDim.x) {
       const IdxTask t = p.idx_tasks[ti];
       const ReqInfo ri = p.reqs[t.req];
@@ -200,45 +232,52 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const int o = tpos >> 7;
       float* srow = scores + ((int64_t)(t.tok0 + row) * p.H + t.h0 + e) * pitch;
       bool ok = true;
-      for (int pg = t.page_begin; pg < t.page_end; ++pg) {
-        const int ab = a_it & 1;
-        if (!mbar_wait(smem_u32(&sm.k_empty[a_it % kKStages]), (a_it / kKStages) & 1, abort_flag,
-                       status)) {
+      for (int pb = t.page_begin; pb < t.page_end; pb += 2, ++jp) {
+        const int ks = jp % kKStages;
+        const bool got = e == 0
+            ? mbar_wait(smem_u32(&sm.a0_full), jp & 1, abort_flag, status)
+            : mbar_wait(smem_u32(&sm.k_empty[ks]), (jp / kKStages) & 1, abort_flag, status);
+        if (!got) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (e < t.nh) {
-          const uint32_t base = tmem + lane_addr + (uint32_t)((ab * 2 + e) * 128);
-          const bool own = valid && pg == o;
-          float mx = -INFINITY;
-          if (__any_sync(0xffffffffu, own)) {
-            const int nvis = own ? (tpos & 127) + 1 : 128;
+          const int npg = min(2, t.page_end - pb);
+          for (int u = 0; u < npg; ++u) {
+            const int pg = pb + u;
+            const uint32_t base = tmem + lane_addr + (uint32_t)(e * 256 + u * 128);
+            const bool own = valid && pg == o;
+            float mx = -INFINITY;
+            if (__any_sync(0xffffffffu, own)) {
+              const int nvis = own ? (tpos & 127) + 1 : 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t v[32];
-              tmem_ld32(base + c * 32, v);
-              tmem_ld_wait();
+              for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(base + c * 32, v);
+                tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (c * 32 + j < nvis) mx = fmaxf(mx, __uint_as_float(v[j]));
+                for (int j = 0; j < 32; ++j)
+                  if (c * 32 + j < nvis) mx = fmaxf(mx, __uint_as_float(v[j]));
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                const float red = tmem_ld32_max(base + c * 32, v);
+                tmem_ld_wait();
+                mx = fmaxf(mx, red);
+              }
             }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t v[32];
-              const float red = tmem_ld32_max(base + c * 32, v);
-              tmem_ld_wait();
-              mx = fmaxf(mx, red);
-            }
+            if (valid && pg <= o) srow[pg] = mx * qk_scale;
           }
-          if (valid && pg <= o) srow[pg] = mx * qk_scale;
         }
         tc_fence_before();
         __syncwarp();
-        // this accumulator pair is free for page step a_it + 2
-        if (lane == 0) mbar_arrive(smem_u32(&sm.k_full[(a_it + 2) % kKStages]));
-        ++a_it;
+        // this accumulator is free for page pair jp + 1
+        if (lane == 0)
+          mbar_arrive(smem_u32(e == 0 ? &sm.k_full[(jp + 1) % kKStages]
+                                      : &sm.a1_free[(jp + 1) % kKStages]));
       }
       if (!ok) break;
     }
