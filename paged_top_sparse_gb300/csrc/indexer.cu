@@ -8,7 +8,8 @@
 //   * warp 0 (TMA producer): per item, the Q tile of each head (3-D tensor map over
 //     [T][H][D], 128-byte swizzle) into a ring of three one-head slots (the next item's first
 //     head loads while the current item runs); per page pair, the two physical K tiles
-//     (looked up in the page table) stacked into one 256-row operand, in a 2-stage ring;
+//     (looked up in the page table) stacked into one 256-row operand, in a ring of 2 stages
+//     (4 for 128-byte rows);
 //   * warp 1 (MMA issuer, one thread): S_h = Q_h K^T with M = 128 rows and N = 256 keys (two
 //     pages per instruction), FP32 accumulators in TMEM, one 256-column buffer per head.  A
 //     128 x 128 x 16 MMA with both operands in shared memory reads 8 KB in 64 cycles, all of
@@ -31,12 +32,14 @@ namespace sps {
 namespace {
 
 constexpr int kQSlots = 3;     // one-head Q tiles: an item's two heads + the next item's first
-constexpr int kKStages = 2;    // page pairs
 constexpr int kThreads = 320;  // 10 warps
 
 template <int ROWB>  // bytes per Q/K row: 128 or 256
 struct IdxSmem {
   static constexpr int TILE = 128 * ROWB;  // one 128-row tile
+  // page-pair stages: the shorter rows' pairs take half the MMA time and half the space, so
+  // they get a deeper ring to hide the same load latency
+  static constexpr int kKStages = ROWB == 128 ? 4 : 2;
   uint8_t q[kQSlots][TILE];                // [column block][128 rows][128 B]
   uint8_t k[kKStages][2 * TILE];           // [column block][256 rows][128 B], page A then B
   uint64_t q_full[kQSlots], q_empty[kQSlots];
@@ -61,6 +64,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   constexpr int DB = ROWB / 128;       // 128-byte column blocks per row
   constexpr int KSTEPS = DB * 4;       // 32-byte K steps per row
   constexpr int TILE = Smem::TILE;
+  constexpr int kKStages = Smem::kKStages;
   constexpr int CB = 128 * 128;        // bytes of one column block of a 128-row tile
   constexpr uint32_t IDESC2 = idesc_mma(BF16IN, BF16IN, 128, 256, false, false);
   constexpr uint32_t IDESC1 = idesc_mma(BF16IN, BF16IN, 128, 128, false, false);
