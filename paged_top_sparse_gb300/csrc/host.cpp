@@ -126,7 +126,7 @@ struct sps_plan {
           off_page_req = 0, off_idx_tasks = 0, off_chunk_offsets = 0,
           off_qconv = -1, off_kconv = -1, off_vconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
-  int64_t upload_bytes = 0;  // [off_tok_pos, off_tok_pos + upload_bytes) comes from `blob`
+  int64_t upload_bytes = 0;  // [0, upload_bytes) of the workspace comes from `blob`
   std::vector<uint8_t> blob;
 };
 
@@ -307,11 +307,11 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   if (p.kv_dtype == SPS_NVFP4) pl->off_vconv = take(2 * cache_elems);
   pl->ws_bytes = off;
 
-  // the host image of [off_tok_pos, upload_end)
-  pl->upload_bytes = upload_end - pl->off_tok_pos;
+  // the host image of [0, upload_end): the status word and counters (zero), then the metadata
+  pl->upload_bytes = upload_end;
   pl->blob.assign(pl->upload_bytes, 0);
   auto put = [&](int64_t o, const void* src, size_t n) {
-    if (n) memcpy(pl->blob.data() + (o - pl->off_tok_pos), src, n);
+    if (n) memcpy(pl->blob.data() + o, src, n);
   };
   put(pl->off_tok_pos, tok_pos.data(), 4 * tok_pos.size());
   put(pl->off_tok_req, tok_req.data(), 4 * tok_req.size());
@@ -413,9 +413,8 @@ sps_status sps_plan_upload(const sps_plan* pl, void* ws, size_t ws_bytes, sps_st
                 (long long)pl->ws_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);  // status + counters
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
-  e = g_staging.upload(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes, s);
+  // one copy: zeroed status word and counters, then the plan metadata
+  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   return SPS_OK;
 }
@@ -786,12 +785,10 @@ sps_status sps_internal_fwd_noalloc(const sps_plan* pl, const void* q, float q_s
                 (long long)pl->ws_bytes, scratch_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(scratch);
-  // the array keeps the previous call's contents: zero the status word and counters, then
-  // write this plan's metadata over the old one
-  cudaError_t e = cudaMemsetAsync(base, 0, pl->off_tok_pos, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch header)");
-  e = g_staging.upload(base + pl->off_tok_pos, pl->blob.data(), pl->upload_bytes, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan metadata -> scratch)");
+  // the array keeps the previous call's contents: one copy zeroes the status word and
+  // counters and writes this plan's metadata over the old one
+  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "plan metadata -> scratch");
   DevPlan d = make_dev_plan(pl, scratch);
   if (dev_status) d.status = dev_status;
   e = launch_inversion(d, idx, lse, lse_split_stride, s);
