@@ -6,7 +6,9 @@ BF16 prefill workload (32 query / 2 KV heads, head dim 128, 128-token pages, top
 permuted physical pages).  Inputs are resident in HBM before timing; L2 is flushed
 (256 MB write) between timed steps and each step is timed with CUDA events on the launching
 stream.  ``e2e`` repeats the step through the same C-ABI calls starting from pinned host
-buffers (H2D of Q/K/V/page table and D2H of the output inside the timed region).
+buffers (H2D of Q/K/V/page table and D2H of the output inside the timed region), with each
+step's copies on their own streams overlapping the neighbouring steps' compute; the serial
+form (copy in, step, copy out, one after another) is reported beside it.
 
 ``--impl reference`` times the FP64 CPU oracle instead (a bounded row sample per step).
 
@@ -67,6 +69,13 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_ready(self, timeout_s: float = 10.0):
+        """Blocks until nvidia-smi has printed its first sample: starting it (NVML setup) must
+        not overlap the timed region."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -192,6 +201,9 @@ def _timed_loop(args, world, dev, flush, step, nseg):
     import torch
 
     stream = torch.cuda.current_stream()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    clocks.wait_ready()
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
@@ -201,21 +213,25 @@ def _timed_loop(args, world, dev, flush, step, nseg):
             import torch.distributed as dist
             dist.barrier()
 
-    clocks = ClockSampler(dev.index)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
            for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    clocks.start()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(float(i))
         step(evs[i])
+    t_enq = time.perf_counter() - t_wall0
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     barrier()
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nseg)]
                     for i in range(args.steps)])  # ms
+    # device time between one step's last event and the next step's first (the L2 flush, plus
+    # any wait for the host)
+    gaps = [evs[i][nseg].elapsed_time(evs[i + 1][0]) for i in range(args.steps - 1)]
+    clocks.host = {"enqueue_ms_per_step": round(t_enq * 1e3 / args.steps, 4),
+                   "between_steps_ms": round(float(np.mean(gaps)), 4) if gaps else None}
     return per, clocks, t_wall, stream
 
 
@@ -240,6 +256,52 @@ def _e2e(args, flush, stream, copy_in, step, copy_out):
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
     return float(np.mean(e_ms))
+
+
+def _e2e_pipelined(args, flush, stream, copy_in, step, copy_out, nbuf=2):
+    """End-to-end throughput with the copies overlapped: every step's H2D copy runs on its
+    own stream (into one of `nbuf` device input sets) and its D2H copy on another, while the
+    launching stream computes the neighbouring steps.  All copies of the K timed steps are
+    inside the timed region (events from the first H2D to the last D2H)."""
+    import torch
+
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    used = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
+    read = [torch.cuda.Event() for _ in range(nbuf)]   # D2H of the set's last output done
+
+    def run(n, first=None):
+        for i in range(n):
+            b = i % nbuf
+            if i >= nbuf:
+                h2d_s.wait_event(used[b])
+            if i == 0 and first is not None:
+                first.record(h2d_s)
+            with torch.cuda.stream(h2d_s):
+                copy_in(b)
+            in_ready[b].record(h2d_s)
+            stream.wait_event(in_ready[b])
+            if i >= nbuf:
+                stream.wait_event(read[b])
+            with torch.cuda.stream(stream):
+                flush.fill_(float(i))
+                step(b)
+            used[b].record(stream)
+            d2h_s.wait_event(used[b])
+            with torch.cuda.stream(d2h_s):
+                copy_out(b)
+            read[b].record(d2h_s)
+        return read[(n - 1) % nbuf]
+
+    run(max(1, args.warmup))
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    last = run(args.steps, first=t0)
+    stream.wait_event(last)
+    t1.record(stream)
+    t1.synchronize()
+    return t0.elapsed_time(t1) / args.steps
 
 
 def run_gpu(args, rank, world):
@@ -287,7 +349,7 @@ def run_gpu(args, rank, world):
         fwd_call = B.sparse_prefill_fwd_fp8qk
     combine_call = B.partial_combine_bf16 if bf16p else B.partial_combine
 
-    def step(ev, di=din):
+    def step(ev, di=din, out_=out):
         pl = B.Plan(*plan_args, **plan_kw)
         if ev: ev[0].record(stream)
         B.sps_plan_upload(pl, ws)
@@ -303,7 +365,7 @@ def run_gpu(args, rank, world):
         fwd_call(pl, di["q"], q_scale, di["k"], di["v"], di.get("k_scales"),
                  di.get("v_scales"), di["pt"], idx, partial, lse, ws)
         if ev: ev[3].record(stream)
-        combine_call(partial, lse, out)
+        combine_call(partial, lse, out_)
         if ev: ev[4].record(stream)
         return pl
 
@@ -321,11 +383,22 @@ def run_gpu(args, rank, world):
         for k_, h_ in hin.items():
             dcopy[k_].copy_(h_, non_blocking=True)
 
-    e2e_ms = _e2e(args, flush, stream, copy_in, lambda ev: step(ev, dcopy),
-                  lambda: hout.copy_(out, non_blocking=True))
+    e2e_serial_ms = _e2e(args, flush, stream, copy_in, lambda ev: step(ev, dcopy),
+                         lambda: hout.copy_(out, non_blocking=True))
+    dsets = [{k: torch.empty_like(x, device=dev) for k, x in hin.items()} for _ in range(2)]
+    douts = [torch.empty_like(out) for _ in range(2)]
+
+    def copy_in_b(b):
+        for k_, h_ in hin.items():
+            dsets[b][k_].copy_(h_, non_blocking=True)
+
+    e2e_ms = _e2e_pipelined(args, flush, stream, copy_in_b,
+                            lambda b: step(None, dsets[b], douts[b]),
+                            lambda b: hout.copy_(douts[b], non_blocking=True))
+    assert torch.equal(douts[(args.steps - 1) % 2], out), "pipelined e2e output differs"
     clk = clocks.stop()
 
-    step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], world)
+    step_ms, e2e_ms, e2e_serial_ms = max_over_ranks([step_ms, e2e_ms, e2e_serial_ms], world)
 
     alg = _algorithmic(w, idx.cpu().numpy(), partial_bytes=2 if bf16p else 4)
     hbm, bf16, peak_kind = _peaks()
@@ -386,12 +459,18 @@ def run_gpu(args, rank, world):
         "fwd_tensor_pipe_frac": kern["fwd"]["tensor_frac"],
         "e2e": {"value": round(job_tokens_per_s(w.num_tokens, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        # indexer, top-k, 5 inversion kernels, forward, combine; plus the dequant kernels of
-        # the quantised path (2 before the indexer, 3 before the forward)
-        "gpu_launches": (14 if w.kv_dtype == "nvfp4" else 9) * args.steps,
+                "d2h_bytes_per_step": d2h,
+                "mode": "pipelined: each step's H2D and D2H on their own streams, overlapping "
+                        "the neighbouring steps' compute; all copies inside the timed region",
+                "serial_ms_per_step": round(e2e_serial_ms, 4),
+                "serial_value": round(job_tokens_per_s(w.num_tokens, world, e2e_serial_ms), 1)},
+        # indexer, top-k, 3 inversion kernels, forward, combine; plus the dequant kernels of
+        # the quantised path (2 before the indexer; 3 before the forward, or 2 on the FP8 route)
+        "gpu_launches": (7 + ((4 if args.fp8qk else 5) if w.kv_dtype == "nvfp4" else 0))
+                        * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
+        "host": clocks.host,
     }
     return line, w, t
 
@@ -463,6 +542,7 @@ def run_combine_stress(args, rank, world, dev):
         "gpu_launches": args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
+        "host": clocks.host,
     }
     return line, None, None
 
@@ -536,6 +616,7 @@ def run_kv_append(args, rank, world, dev):
         "gpu_launches": args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
+        "host": clocks.host,
     }
     return line, None, None
 
