@@ -316,6 +316,210 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   }
 }
 
+// Grid-wide barrier of a cooperative launch (every block resident).  Arrivals count up in
+// bar[0]; the last block resets it and advances the generation in bar[1], which the others
+// wait for.  The wait gives up after the library's wait limit, raising DEV_TIMEOUT, and the
+// block then returns false so the kernel ends instead of hanging.
+__device__ __forceinline__ bool grid_barrier(unsigned int* bar, int32_t* status, int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* gen = bar + 1;
+    const unsigned int g = *gen;
+    __threadfence();
+    int ok = 1;
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (*gen == g) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_status(status, DEV_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *flag = ok;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// All the steps in one cooperative launch, one block per chunk (as count_kernel): the page
+// masks of every window stay in shared memory and the row's selections in registers from
+// the count to the emit, and two grid barriers replace the kernel boundaries.  After the
+// second, every block scans the bucket totals itself, so no single block has to publish the
+// bucket offsets before the others can emit.
+template <int KV>
+__global__ void __launch_bounds__(256, 8)
+fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
+             int64_t lse_split_stride, int nwin) {
+  extern __shared__ uint32_t dyn[];
+  uint32_t (*tmw)[kInvPages][kChunkWords + 1] =
+      reinterpret_cast<uint32_t (*)[kInvPages][kChunkWords + 1]>(dyn);  // [nwin]
+  __shared__ int pos0[kInvPages][kChunkWords + 1];
+  __shared__ int sh[32];
+  __shared__ int flag;
+  unsigned int* bar = reinterpret_cast<unsigned int*>(p.counters + 4);
+  int g = 0, c = 0;
+  const int b = find_block(p, blockIdx.x, &g, &c);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_task = kFwdTaskGroups * 128;
+  // ---- 1. count
+  RowCtx rc{};
+  RowSel<KV> sel;
+  const ReqInfo* ri = b >= 0 ? &p.reqs[b] : nullptr;
+  if (ri) {
+    rc = row_of(p, *ri, g, c * kChunkWords + warp, lane);
+    sel.load(idx, rc, p.K);
+    if (rc.valid) {
+#pragma unroll
+      for (int s = 0; s < sel.n(); ++s) {
+        if (s >= p.K) break;
+        const int pg = sel.get(s);
+        if (pg < 0) lse[s * lse_split_stride + rc.r] = -INFINITY;
+        else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
+      }
+    }
+    for (int wi = 0; wi * kInvPages < ri->npages; ++wi)
+      masks_to_smem(tmw[wi], row_mask(sel, rc, wi * kInvPages), warp, lane);
+    __syncthreads();
+    for (int wi = 0; wi * kInvPages < ri->npages; ++wi) {
+      const int d = threadIdx.x, p0 = wi * kInvPages;
+      if (d < kInvPages && p0 + d < ri->npages) {
+        int n = 0;
+#pragma unroll 8
+        for (int v = 0; v < kChunkWords; ++v) n += __popc(tmw[wi][d][v]);
+        p.chunk_offsets[chunk_id(p, *ri, p0 + d, g, c)] = n;
+      }
+    }
+  }
+  if (!grid_barrier(bar, p.status, &flag)) return;
+  // ---- 2. chunk offsets within each bucket, bucket totals
+  for (int bk = blockIdx.x; bk < p.num_buckets; bk += gridDim.x) {
+    const int gp = bk / p.Hkv, gg = bk % p.Hkv;
+    const ReqInfo& rb = p.reqs[p.page_req[gp]];
+    int32_t* cnt = p.chunk_offsets + chunk_id(p, rb, gp - rb.page_base, gg, 0);
+    const int n = rb.ch_per_bucket;
+    const int per = (n + 255) / 256;
+    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+    int x = 0;
+    for (int i = i0; i < i1; ++i) x += __ldcg(cnt + i);
+    int off;
+    const int total = block_exclusive_scan(x, &off, sh);
+    for (int i = i0; i < i1; ++i) {
+      const int v = __ldcg(cnt + i);
+      cnt[i] = off;
+      off += v;
+    }
+    if (threadIdx.x == 0) p.bucket_totals[bk] = total;
+  }
+  if (!grid_barrier(bar, p.status, &flag)) return;
+  // ---- 3. every block: exclusive scans over the bucket totals (entries and work items).
+  // Each thread walks its run of buckets once: it keeps the CSR offsets of this block's own
+  // buckets (its request and KV head, every page) for the emit, and writes the offset and
+  // work items of every gridDim-th bucket.
+  __shared__ int s_boff[512];  // CSR offset of page pg's bucket of this block's KV head
+  {
+    const int nb = p.num_buckets;
+    const int per = (nb + 255) / 256;
+    const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
+    int cnt = 0, ntask = 0;
+    for (int bk = b0; bk < b1; ++bk) {
+      const int t = __ldcg(p.bucket_totals + bk);
+      cnt += t;
+      ntask += (t + per_task - 1) / per_task;
+    }
+    int o, to;
+    const int total = block_exclusive_scan(cnt, &o, sh);
+    const int ttotal = block_exclusive_scan(ntask, &to, sh);
+    const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
+    for (int bk = b0; bk < b1; ++bk) {
+      const int t = __ldcg(p.bucket_totals + bk);
+      const int nt = (t + per_task - 1) / per_task;
+      if (bk % (int)gridDim.x == (int)blockIdx.x) {
+        p.bucket_offsets[bk] = o;
+        for (int j = 0; j < nt; ++j) {
+          if (to + j < p.max_fwd_tasks) {
+            FwdTask ft;
+            ft.bucket = bk;
+            ft.entry_begin = o + j * per_task;
+            ft.count = min(per_task, t - j * per_task);
+            ft.pad = 0;
+            p.fwd_tasks[to + j] = ft;
+          }
+        }
+      }
+      if (ri && bk >= own0 && (bk - own0) % p.Hkv == 0 && (bk - own0) / p.Hkv < ri->npages)
+        s_boff[(bk - own0) / p.Hkv] = o;
+      o += t;
+      to += nt;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      p.bucket_offsets[nb] = total;
+      if (total > p.max_entries) set_status(p.status, DEV_OVERFLOW);
+      p.counters[2] = min(ttotal, p.max_fwd_tasks);
+      if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
+    }
+  }
+  __syncthreads();
+  // ---- 4. emit
+  if (!ri) return;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int wi = 0; wi * kInvPages < ri->npages; ++wi) {
+    const int d = threadIdx.x, p0 = wi * kInvPages;
+    if (d < kInvPages && p0 + d < ri->npages) {
+      int acc = s_boff[p0 + d] + __ldcg(p.chunk_offsets + chunk_id(p, *ri, p0 + d, g, c));
+      for (int v = 0; v < kChunkWords; ++v) {
+        pos0[d][v] = acc;
+        acc += __popc(tmw[wi][d][v]);
+      }
+    }
+    __syncthreads();
+    if (rc.valid) {
+#pragma unroll
+      for (int s = 0; s < sel.n(); ++s) {
+        const int pg = sel.get(s);
+        const int dd = pg - p0;
+        if (dd < 0 || dd >= kInvPages || pg > rc.o) continue;
+        const int pos = pos0[dd][warp] + __popc(tmw[wi][dd][warp] & below);
+        p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int KV>
+bool try_fused(const DevPlan& p, const int32_t* idx, float* lse, int64_t lse_split_stride,
+               cudaStream_t st, cudaError_t* err) {
+  // max_pages bounds every request's page count, so it sizes the 64-page windows
+  const int nwin = (p.max_pages + kInvPages - 1) / kInvPages;
+  const size_t dsmem = (size_t)nwin * kInvPages * (kChunkWords + 1) * sizeof(uint32_t);
+  auto kern = fused_kernel<KV>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, dsmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  if ((int64_t)per_sm * num_sms() < p.inv_blocks || p.inv_blocks < 1) return false;
+  DevPlan pc = p;
+  int64_t lss = lse_split_stride;
+  int nw = nwin;
+  void* args[] = {&pc, const_cast<int32_t**>(&idx), &lse, &lss, &nw};
+  *err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(p.inv_blocks),
+                                     dim3(256), args, dsmem, st);
+  if (*err == cudaErrorCooperativeLaunchTooLarge) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
@@ -323,6 +527,10 @@ cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
   cudaError_t e;
   // selections held in registers when top_k is a multiple of 4 up to 16
   const int kv = (p.K % 4 == 0 && p.K <= 16) ? 16 : 0;
+  // one cooperative launch when every chunk's block fits on the GPU at once
+  if (kv == 16 ? try_fused<16>(p, idx, lse, lse_split_stride, st, &e)
+               : try_fused<0>(p, idx, lse, lse_split_stride, st, &e))
+    return e;
   const unsigned nblk = (unsigned)p.inv_blocks;
   if (nblk > 0) {
     if (kv == 16) count_kernel<16><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);

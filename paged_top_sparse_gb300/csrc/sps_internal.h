@@ -57,6 +57,7 @@ struct DevPlan {
   int32_t num_chunks;       // inversion chunks (buckets x chunks per bucket)
   int32_t* chunk_offsets;   // [num_chunks + 1]: entries before each chunk
   int32_t* bucket_offsets;  // [num_buckets + 1]
+  int32_t* bucket_totals;   // [num_buckets]: entries per bucket (single-launch inversion)
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
   // FP16 copies of quantised inputs (null when the plan has none): Q [T][H][D] and K, V
