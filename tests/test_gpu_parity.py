@@ -541,3 +541,26 @@ def test_bounded_wait_times_out_without_hanging():
     B.partial_combine(part, lse, out)
     torch.cuda.synchronize()
     assert torch.allclose(out.float(), part.mean(0), atol=2e-2)
+
+
+def test_inversion_when_the_single_launch_does_not_fit():
+    """12000 tokens x 16 heads per KV group: 1500 inversion chunks, more blocks than the GPU
+    holds at once, so the inversion takes its three-kernel path; the CSR offsets and entries
+    must still match the oracle bit for bit (and the 8K workloads above cover the
+    single-launch path)."""
+    from tests.gpu_helpers import DeviceRun
+
+    w = synth.workload("custom", seed=31, q_lens=[12000], ctx_lens=[0], num_q_heads=32,
+                       num_kv_heads=2, head_dim=128, top_k=16)
+    run = DeviceRun(w, synth.make_tensors(w))
+    run.run_all()
+    assert run.status() == 0
+    idx_all = run.idx.cpu().numpy()
+    offsets, er, es = orc.inversion(oracle_problem(w), idx_all)
+    info = run.plan.info()
+    nb = len(offsets) - 1
+    got_off = run.ws_array(info.off_bucket_offsets, nb + 1, np.int32)
+    assert np.array_equal(got_off, offsets.astype(np.int32))
+    ent = run.ws_array(info.off_entries, 2 * len(er), np.int32).reshape(-1, 2)
+    assert np.array_equal(ent[:, 0], er)
+    assert np.array_equal(ent[:, 1] & 63, es)
