@@ -405,6 +405,11 @@ def run_gpu(args, rank, world):
     idx_peak = bf16 * 2 if idx_fp8 else bf16  # FP8 tensor rate: the nominal 2x of BF16
     k_ms = per.mean(0)
     names = ["indexer", "topk", "fwd", "combine"]
+    # the inversion is one cooperative launch when its 256-row blocks fit on the GPU at once
+    # (8 per SM), else three kernels
+    hg = w.num_q_heads // w.num_kv_heads
+    inv_blocks = sum(w.num_kv_heads * -(-(-(-ql * hg // 32)) // 8) for ql in w.q_lens)
+    inv_launches = 1 if inv_blocks <= 8 * torch.cuda.get_device_properties(dev).multi_processor_count else 3
     kern = {
         "indexer": {"us": k_ms[0] * 1e3, "achieved": alg["indexer_flops"] / (k_ms[0] * 1e-3) / 1e12,
                     "unit": "TFLOP/s", "peak": idx_peak, "bound": "tensor"},
@@ -464,9 +469,10 @@ def run_gpu(args, rank, world):
                         "the neighbouring steps' compute; all copies inside the timed region",
                 "serial_ms_per_step": round(e2e_serial_ms, 4),
                 "serial_value": round(job_tokens_per_s(w.num_tokens, world, e2e_serial_ms), 1)},
-        # indexer, top-k, 3 inversion kernels, forward, combine; plus the dequant kernels of
-        # the quantised path (2 before the indexer; 3 before the forward, or 2 on the FP8 route)
-        "gpu_launches": (7 + ((4 if args.fp8qk else 5) if w.kv_dtype == "nvfp4" else 0))
+        # indexer, top-k, the inversion, forward, combine; plus the dequant kernels of the
+        # quantised path (2 before the indexer; 3 before the forward, or 2 on the FP8 route)
+        "gpu_launches": (4 + inv_launches
+                         + ((4 if args.fp8qk else 5) if w.kv_dtype == "nvfp4" else 0))
                         * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
