@@ -361,6 +361,16 @@ sps_status sparse_prefill_fwd_noalloc(const sps_plan* plan, const void* q, float
 sps_status sps_check_wait_timeout(int64_t limit_ns, int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sps_check_barrier_timeout -- the same check for the grid barrier of the library's
+ * cooperative launch (the single-launch inversion inside sparse_prefill_fwd): two blocks, one
+ * of which leaves without arriving, so the other's barrier wait must give up after
+ * `limit_ns` (1 ms .. 10 s), record SPS_DEV_TIMEOUT in *dev_status and return.
+ *   dev_barrier  device uint32[2], zeroed by the caller (the barrier's counters)
+ */
+sps_status sps_check_barrier_timeout(int64_t limit_ns, uint32_t* dev_barrier,
+                                     int32_t* dev_status, sps_stream_t stream);
+
+/*
  * sps_read_device_status -- synchronous: waits for the device, then copies the plan
  * workspace's status word into *code (SPS_DEV_*).  Returns SPS_EDEVICE when it is non-zero.
  */

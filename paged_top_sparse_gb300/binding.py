@@ -96,10 +96,12 @@ def lib(path: str | None = None):
     L.sps_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     L.sps_dequantize.argtypes = [ctypes.c_int, vp, vp, i64, vp, vp]
     L.sps_check_wait_timeout.argtypes = [i64, vp, vp]
+    L.sps_check_barrier_timeout.argtypes = [i64, vp, vp, vp]
     L.sps_last_error.restype = ctypes.c_char_p
     for name in ("sparse_prefill_plan", "sps_plan_get_info", "sps_plan_upload", "indexer_scores",
                  "topk_select", "sparse_prefill_fwd", "partial_combine", "sps_read_device_status",
-                 "sparse_prefill_fwd_noalloc", "sps_dequantize", "sps_check_wait_timeout"):
+                 "sparse_prefill_fwd_noalloc", "sps_dequantize", "sps_check_wait_timeout",
+                 "sps_check_barrier_timeout"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -261,6 +263,12 @@ def sps_dequantize(in_dtype: str, data, scales, n: int, out_f16, stream=None):
 def sps_check_wait_timeout(limit_ns: int, dev_status, stream=None):
     """Launch the bounded-wait self-check; *dev_status becomes SPS_DEV_TIMEOUT (1)."""
     _check(lib().sps_check_wait_timeout(int(limit_ns), _ptr(dev_status), _stream(stream)))
+
+
+def sps_check_barrier_timeout(limit_ns: int, dev_barrier, dev_status, stream=None):
+    """Grid-barrier timeout self-check: dev_barrier is a zeroed device int32 tensor of 2."""
+    _check(lib().sps_check_barrier_timeout(int(limit_ns), _ptr(dev_barrier), _ptr(dev_status),
+                                           _stream(stream)))
 
 
 def sps_read_device_status(plan: Plan, workspace) -> int:

@@ -493,9 +493,9 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
     return fail(SPS_EUNSUPPORTED, "sparse_prefill_fwd_fp8qk: needs E4M3 Q, NVFP4 K/V, D = 128");
   DevPlan d = make_dev_plan(pl, ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // counters [1] (forward task cursor), [2] (task count) and [3] (inversion buckets scanned)
-  // start at zero
-  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 3 * sizeof(int32_t), s);
+  // counters [1] (forward task cursor), [2] (task count), [3] (inversion buckets scanned) and
+  // [4], [5] (the single-launch inversion's grid barrier) start at zero
+  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 5 * sizeof(int32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
   e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
@@ -663,6 +663,17 @@ sps_status sps_check_wait_timeout(int64_t limit_ns, int32_t* dev_status, sps_str
     return fail(SPS_EINVAL, "sps_check_wait_timeout: limit_ns must be in [1e6, 1e10]");
   return launched(launch_wait_timeout(dev_status, limit_ns, reinterpret_cast<cudaStream_t>(stream)),
                   "wait-timeout check launch");
+}
+
+sps_status sps_check_barrier_timeout(int64_t limit_ns, uint32_t* dev_barrier,
+                                     int32_t* dev_status, sps_stream_t stream) {
+  if (!dev_status || !aligned(dev_status, 4) || !dev_barrier || !aligned(dev_barrier, 4))
+    return fail(SPS_EINVAL, "sps_check_barrier_timeout: dev_barrier/dev_status must be device words");
+  if (limit_ns < 1000000 || limit_ns > 10000000000LL)
+    return fail(SPS_EINVAL, "sps_check_barrier_timeout: limit_ns must be in [1e6, 1e10]");
+  return launched(launch_barrier_timeout(dev_barrier, dev_status, limit_ns,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                  "barrier timeout check launch");
 }
 
 sps_status sps_read_device_status(const sps_plan* pl, const void* ws, int32_t* code) {

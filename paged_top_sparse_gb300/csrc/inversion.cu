@@ -316,39 +316,6 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   }
 }
 
-// Grid-wide barrier of a cooperative launch (every block resident).  Arrivals count up in
-// bar[0]; the last block resets it and advances the generation in bar[1], which the others
-// wait for.  The wait gives up after the library's wait limit, raising DEV_TIMEOUT, and the
-// block then returns false so the kernel ends instead of hanging.
-__device__ __forceinline__ bool grid_barrier(unsigned int* bar, int32_t* status, int* flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    volatile unsigned int* gen = bar + 1;
-    const unsigned int g = *gen;
-    __threadfence();
-    int ok = 1;
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (*gen == g) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          set_status(status, DEV_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    __threadfence();
-    *flag = ok;
-  }
-  __syncthreads();
-  return *flag != 0;
-}
-
 // All the steps in one cooperative launch, one block per chunk (as count_kernel): the page
 // masks of every window stay in shared memory and the row's selections in registers from
 // the count to the emit, and two grid barriers replace the kernel boundaries.  After the

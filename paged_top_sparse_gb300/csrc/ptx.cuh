@@ -84,6 +84,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Grid-wide barrier of a cooperative launch (every block resident).  Arrivals count up in
+// bar[0]; the last block resets it and advances the generation in bar[1], which the others
+// wait for.  The wait gives up after `limit_ns` (the library's wait limit), raising
+// DEV_TIMEOUT, and the block then returns false so the kernel ends instead of hanging.
+// bar[0..1] start at zero.
+__device__ __forceinline__ bool grid_barrier(unsigned int* bar, int32_t* status, int* flag,
+                                             uint64_t limit_ns = kWaitLimitNs) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* gen = bar + 1;
+    const unsigned int g = *gen;
+    __threadfence();
+    int ok = 1;
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (*gen == g) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+          set_status(status, DEV_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *flag = ok;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
 // ------------------------------------------------------------------ TMA / bulk copies
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");

@@ -48,7 +48,8 @@ struct DevPlan {
   float sm_scale;
   int32_t* status;
   int32_t* counters;        // [0] indexer task cursor, [1] forward task cursor, [2] fwd task
-                            // count, [3] inversion buckets scanned
+                            // count, [3] inversion buckets scanned, [4] [5] inversion grid
+                            // barrier (arrivals, generation)
   const int32_t* tok_pos;   // [T]
   const int32_t* tok_req;   // [T]
   const ReqInfo* reqs;      // [batch]
@@ -114,6 +115,8 @@ cudaError_t launch_absmax_bf16(const void* in, int64_t n, float* out, cudaStream
 
 // One-block kernel whose bounded wait on a never-arrived mbarrier must time out.
 cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t st);
+cudaError_t launch_barrier_timeout(unsigned int* bar, int32_t* status, int64_t limit_ns,
+                                   cudaStream_t st);
 
 // Exact E4M3 / NVFP4 -> FP16 conversion of n elements (n % 16 == 0).
 cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,

@@ -543,6 +543,29 @@ def test_bounded_wait_times_out_without_hanging():
     assert torch.allclose(out.float(), part.mean(0), atol=2e-2)
 
 
+def test_grid_barrier_times_out_without_hanging():
+    """The cooperative inversion's grid barrier: one of two blocks leaves without arriving, the
+    other's wait ends after its limit with SPS_DEV_TIMEOUT, and the context stays usable."""
+    import time
+
+    from paged_top_sparse_gb300 import binding as B
+
+    bar = torch.zeros(2, dtype=torch.int32, device="cuda:0")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    t0 = time.perf_counter()
+    B.sps_check_barrier_timeout(200_000_000, bar, st)  # 0.2 s
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == 1  # SPS_DEV_TIMEOUT
+    assert 0.15 < dt < 5.0
+    part = torch.randn((2, 64, 128), device="cuda:0")
+    lse = torch.zeros((2, 64), device="cuda:0")
+    out = torch.empty((64, 128), dtype=torch.bfloat16, device="cuda:0")
+    B.partial_combine(part, lse, out)
+    torch.cuda.synchronize()
+    assert torch.allclose(out.float(), part.mean(0), atol=2e-2)
+
+
 def test_inversion_when_the_single_launch_does_not_fit():
     """12000 tokens x 16 heads per KV group: 1500 inversion chunks, more blocks than the GPU
     holds at once, so the inversion takes its three-kernel path; the CSR offsets and entries
