@@ -3,7 +3,7 @@
 // The forward runs one work item per (page, KV head, query split) ("MSA PR 21: Q8KV4 paged
 // sparse prefill", K1), so the row-major selection idx[row][slot] is turned around: for every
 // bucket (request, logical page, KV head) the (row, slot) pairs that chose it, in ascending row
-// order.  Nothing depends on the timing of atomics, and no global atomics are used:
+// order.  Nothing depends on the timing of atomics, and no global atomics touch the data:
 //
 //   1. count    a 256-thread block per (request, KV head, chunk of 256 consecutive rows of
 //               the group), a thread per row.  Per window of 64 pages each thread turns its
@@ -11,16 +11,22 @@
 //               mask, and 64 ballots turn a warp's 32 masks around into one 32-bit row mask per
 //               page; the block sums the popcounts of each page's 8 warp masks into that
 //               (bucket, chunk)'s entry count.  Empty slots get lse = -inf here.
-//   2. chunks   a block per bucket: exclusive scan over the bucket's chunks (bucket-local
-//               offsets) and the bucket's total.  The last block to finish (an atomic ticket
-//               after a memory fence, no waiting) then runs
+//   2. chunks   per bucket: exclusive scan over the bucket's chunks (bucket-local offsets)
+//               and the bucket's total.
 //   3. buckets  exclusive scan over the bucket totals, which gives the CSR offsets, and the
 //               forward's work list (chunks of up to kFwdTaskGroups x 128 entries per bucket).
-//   4. emit     the grid of step 1 rebuilds the same masks; a page's entries of the chunk
-//               start at the bucket's offset plus the chunk's plus the rows of earlier warps,
-//               and a row's entry at that plus the set bits of lower lanes.  An entry is
-//               (row, t * 64 + slot), t the row's absolute position, so the forward needs no
-//               further lookup to find the row's own page and visible key count.
+//   4. emit     a page's entries of the chunk start at the bucket's offset plus the chunk's
+//               plus the rows of earlier warps, and a row's entry at that plus the set bits of
+//               lower lanes.  An entry is (row, t * 64 + slot), t the row's absolute position,
+//               so the forward needs no further lookup to find the row's own page and visible
+//               key count.
+//
+// When every chunk's block fits on the GPU at once (the usual case), one cooperative launch
+// runs all four steps (fused_kernel): the masks stay in shared memory and the selections in
+// registers from step 1 to step 4, two bounded grid barriers separate the steps, and every
+// block does step 3 itself.  Otherwise three kernels run: count, scan (a block per bucket for
+// step 2; the last block to finish, found by an atomic ticket after a memory fence with no
+// waiting, does step 3) and emit (which rebuilds the masks).
 #include "ptx.cuh"
 #include "sps_internal.h"
 
