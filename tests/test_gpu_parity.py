@@ -54,6 +54,13 @@ def _workload(name):
         return synth.workload("custom", seed=16, q_lens=[190], ctx_lens=[70], num_q_heads=2,
                               num_kv_heads=1, head_dim=64, top_k=2, q_dtype="e4m3",
                               kv_dtype="nvfp4")
+    if name == "maxctx":  # the largest page count a plan takes (512 pages, 64K tokens)
+        return synth.workload("custom", seed=41, q_lens=[200], ctx_lens=[65300], num_q_heads=4,
+                              num_kv_heads=2, head_dim=128, top_k=16)
+    if name == "with_empty":  # requests without new tokens between others
+        return synth.workload("custom", seed=42, q_lens=[0, 150, 0, 33],
+                              ctx_lens=[500, 700, 0, 1000], num_q_heads=4, num_kv_heads=2,
+                              head_dim=64, top_k=4)
     if name == "chunked_fp8_small":  # chunked prefill, E4M3 indexer q/k, BF16 attention
         return synth.workload("custom", seed=14, q_lens=[200, 64, 131], ctx_lens=[1000, 2900, 555],
                               num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=6,
@@ -61,7 +68,8 @@ def _workload(name):
     return synth.workload(name, seed=0)
 
 
-SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64"]
+SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64",
+         "maxctx", "with_empty"]
 FULL = ["prefill8k", "prefill8k_q", "chunked32k"]
 _cache = {}
 
