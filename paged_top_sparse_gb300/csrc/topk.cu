@@ -47,7 +47,8 @@ __device__ __forceinline__ void sort_best_first(uint32_t (&k)[E], uint32_t (&pg)
       }
 }
 
-template <int E>  // pages per lane: max_pages <= 32 * E
+// KC: top_k fixed at compile time (the rounds unroll completely), or 0 for any top_k.
+template <int E, int KC = 0>  // pages per lane: max_pages <= 32 * E
 __global__ void __launch_bounds__(256)
 topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t* __restrict__ idx) {
   const int lane = threadIdx.x & 31;
@@ -55,7 +56,7 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
   const int64_t R = (int64_t)p.T * p.H;
   if (r >= R) return;
   const int o = __ldg(p.tok_pos + r / p.H) >> 7;
-  const int n = o + 1, K = p.K;
+  const int n = o + 1, K = KC ? KC : p.K;
   int32_t* out = idx + r * K;
   if (n <= K) {  // every visible page is kept
     for (int s = lane; s < K; s += 32) out[s] = s < n ? s : -1;
@@ -73,7 +74,7 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
   sort_best_first<E>(key, pg);
   const uint32_t lt = (1u << lane) - 1u;
   int c = 0;  // this lane's candidates taken so far: the first c of the sorted order
-#pragma unroll 4
+#pragma unroll (KC ? KC : 4)
   for (int round = 1; round < K; ++round) {
     const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
     const uint32_t tie = __ballot_sync(0xffffffffu, key[0] == m);
@@ -238,11 +239,23 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
   const int64_t R = (int64_t)p.T * p.H;
   const unsigned grid = (unsigned)((R + 7) / 8);
   if (grid == 0) return cudaSuccess;
-  if (p.max_pages <= 32) topk_kernel<1><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else if (p.max_pages <= 64) topk_kernel<2><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else if (p.max_pages <= 128) topk_kernel<4><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else if (p.max_pages <= 256) topk_filter_kernel<8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-  else topk_filter_kernel<16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  // top_k = 16 (the common case) runs instances whose rounds unroll completely (the filtered
+  // long rows do better with the rolled loop)
+  const bool k16 = p.K == 16;
+  if (p.max_pages <= 32) {
+    if (k16) topk_kernel<1, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    else topk_kernel<1><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else if (p.max_pages <= 64) {
+    if (k16) topk_kernel<2, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    else topk_kernel<2><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else if (p.max_pages <= 128) {
+    if (k16) topk_kernel<4, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    else topk_kernel<4><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else if (p.max_pages <= 256) {
+    topk_filter_kernel<8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else {
+    topk_filter_kernel<16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  }
   return cudaGetLastError();
 }
 
