@@ -144,10 +144,11 @@ sps_status sps_plan_get_info(const sps_plan* plan, sps_plan_info* info);
 
 /*
  * sps_plan_upload -- copies the plan's metadata into `workspace` (device, >= workspace_bytes,
- * 256-byte aligned) on `stream` and clears the device status word.  Call once per (plan,
- * workspace) before the other plan calls, on the same stream, and outside CUDA graph capture
- * (the source is pageable host memory: the call returns once the bytes are staged, so the
- * plan may be destroyed afterwards).
+ * 256-byte aligned) on `stream` with one host-to-device copy that also clears the device status
+ * word and counters.  Call once per (plan, workspace) before the other plan calls, on the same
+ * stream, and outside CUDA graph capture.  The bytes go through a page-locked staging ring of
+ * the library (a region is reused only after the event behind its copy has completed), so the
+ * copy is a plain asynchronous DMA and the plan may be destroyed as soon as the call returns.
  */
 sps_status sps_plan_upload(const sps_plan* plan, void* workspace, size_t workspace_bytes,
                            sps_stream_t stream);
