@@ -258,29 +258,49 @@ def _e2e(args, flush, stream, copy_in, step, copy_out):
     return float(np.mean(e_ms))
 
 
-def _e2e_pipelined(args, flush, stream, copy_in, step, copy_out, nbuf=2):
-    """End-to-end throughput with the copies overlapped: every step's H2D copy runs on its
-    own stream (into one of `nbuf` device input sets) and its D2H copy on another, while the
-    launching stream computes the neighbouring steps.  All copies of the K timed steps are
-    inside the timed region (events from the first H2D to the last D2H)."""
+def _byte_chunks(pairs, chunk_bytes=16 << 20):
+    """Split (device dst, pinned host src) tensor pairs into byte slices of at most chunk_bytes."""
     import torch
 
-    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-    in_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    out = []
+    for d, h in pairs:
+        db, hb = d.reshape(-1).view(torch.uint8), h.reshape(-1).view(torch.uint8)
+        for i in range(0, hb.numel(), chunk_bytes):
+            out.append((db[i:i + chunk_bytes], hb[i:i + chunk_bytes]))
+    return out
+
+
+def _e2e_pipelined(args, flush, stream, in_pairs, step, copy_out, nbuf=2):
+    """End-to-end throughput with the copies overlapped: every step's H2D copies run on their
+    own streams (`--h2d-streams` of them, the inputs cut into 16 MB slices dealt round-robin,
+    into one of `nbuf` device input sets) and its D2H copy on another, while the launching
+    stream computes the neighbouring steps.  All copies of the K timed steps are inside the
+    timed region (events from the first H2D to the last D2H)."""
+    import torch
+
+    nh = max(1, args.h2d_streams)
+    h2d_s = [torch.cuda.Stream() for _ in range(nh)]
+    d2h_s = torch.cuda.Stream()
+    slices = [_byte_chunks(in_pairs(b)) for b in range(nbuf)]
+    in_ready = [[torch.cuda.Event() for _ in range(nh)] for _ in range(nbuf)]
     used = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
     read = [torch.cuda.Event() for _ in range(nbuf)]   # D2H of the set's last output done
 
     def run(n, first=None):
         for i in range(n):
             b = i % nbuf
-            if i >= nbuf:
-                h2d_s.wait_event(used[b])
             if i == 0 and first is not None:
-                first.record(h2d_s)
-            with torch.cuda.stream(h2d_s):
-                copy_in(b)
-            in_ready[b].record(h2d_s)
-            stream.wait_event(in_ready[b])
+                first.record(h2d_s[0])
+                for s_ in h2d_s[1:]:
+                    s_.wait_event(first)
+            for j, s_ in enumerate(h2d_s):
+                if i >= nbuf:
+                    s_.wait_event(used[b])
+                with torch.cuda.stream(s_):
+                    for d_, h_ in slices[b][j::nh]:
+                        d_.copy_(h_, non_blocking=True)
+                in_ready[b][j].record(s_)
+                stream.wait_event(in_ready[b][j])
             if i >= nbuf:
                 stream.wait_event(read[b])
             with torch.cuda.stream(stream):
@@ -388,11 +408,8 @@ def run_gpu(args, rank, world):
     dsets = [{k: torch.empty_like(x, device=dev) for k, x in hin.items()} for _ in range(2)]
     douts = [torch.empty_like(out) for _ in range(2)]
 
-    def copy_in_b(b):
-        for k_, h_ in hin.items():
-            dsets[b][k_].copy_(h_, non_blocking=True)
-
-    e2e_ms = _e2e_pipelined(args, flush, stream, copy_in_b,
+    e2e_ms = _e2e_pipelined(args, flush, stream,
+                            lambda b: [(dsets[b][k_], h_) for k_, h_ in hin.items()],
                             lambda b: step(None, dsets[b], douts[b]),
                             lambda b: hout.copy_(douts[b], non_blocking=True))
     assert torch.equal(douts[(args.steps - 1) % 2], out), "pipelined e2e output differs"
@@ -465,13 +482,15 @@ def run_gpu(args, rank, world):
         "e2e": {"value": round(job_tokens_per_s(w.num_tokens, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "mode": "pipelined: each step's H2D and D2H on their own streams, overlapping "
-                        "the neighbouring steps' compute; all copies inside the timed region",
+                "mode": f"pipelined: each step's H2D ({args.h2d_streams} stream(s)) and D2H on "
+                        "their own streams, overlapping the neighbouring steps' compute; all "
+                        "copies inside the timed region",
                 "serial_ms_per_step": round(e2e_serial_ms, 4),
                 "serial_value": round(job_tokens_per_s(w.num_tokens, world, e2e_serial_ms), 1)},
-        # indexer, top-k, the inversion, forward, combine; plus the dequant kernels of the
-        # quantised path (2 before the indexer; 3 before the forward, or 2 on the FP8 route)
-        "gpu_launches": (4 + inv_launches
+        # plan-upload copy, indexer, top-k, the inversion, forward, combine; plus the dequant
+        # kernels of the quantised path (2 before the indexer; 3 before the forward, or 2 on
+        # the FP8 route)
+        "gpu_launches": (5 + inv_launches
                          + ((4 if args.fp8qk else 5) if w.kv_dtype == "nvfp4" else 0))
                         * args.steps,
         "clocks": clk,
@@ -693,6 +712,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--h2d-streams", type=int, default=1,
+                    help="streams that share each step's host-to-device input copies in the "
+                         "pipelined end-to-end measurement")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="prefill length (8192 = the benchmark workload; others for profiling)")
     ap.add_argument("--workload", default="prefill8k", choices=WORKLOADS,

@@ -144,11 +144,14 @@ sps_status sps_plan_get_info(const sps_plan* plan, sps_plan_info* info);
 
 /*
  * sps_plan_upload -- copies the plan's metadata into `workspace` (device, >= workspace_bytes,
- * 256-byte aligned) on `stream` with one host-to-device copy that also clears the device status
- * word and counters.  Call once per (plan, workspace) before the other plan calls, on the same
- * stream, and outside CUDA graph capture.  The bytes go through a page-locked staging ring of
- * the library (a region is reused only after the event behind its copy has completed), so the
- * copy is a plain asynchronous DMA and the plan may be destroyed as soon as the call returns.
+ * 256-byte aligned) on `stream` with one copy that also clears the device status word and
+ * counters.  Call once per (plan, workspace) before the other plan calls, on the same stream,
+ * and outside CUDA graph capture; call it again after the status word has recorded an error.
+ * The bytes go through a mapped page-locked staging ring of the library (allocated on the first
+ * call; a region is reused only after the event behind its copy has completed) and a small
+ * copy kernel on `stream` reads them from there, so the upload never waits for the caller's
+ * own host<->device transfers on other streams, and the plan may be destroyed as soon as the
+ * call returns.  Where the ring cannot be allocated or mapped it is a plain asynchronous copy.
  */
 sps_status sps_plan_upload(const sps_plan* plan, void* workspace, size_t workspace_bytes,
                            sps_stream_t stream);
@@ -328,7 +331,9 @@ sps_status sps_dequantize(sps_dtype in_dtype, const void* in, const void* scales
  * Arguments are those of sparse_prefill_fwd without the workspace, plus
  *   dev_status  device int32 or NULL: where the kernels record device-side errors
  *               (SPS_DEV_*; the caller clears it).  With NULL such errors go unreported.
- * The plan needs no sps_plan_upload: this call copies the plan's metadata into the array.
+ * The plan needs no sps_plan_upload: this call copies the plan's metadata into the array
+ * (through the library's staging ring when an earlier call has allocated it, else as a plain
+ * asynchronous copy from the plan's own host memory; it never allocates the ring).
  *
  * Rules.
  *   - The array holds 48 MiB per device and every GPU that loads the library keeps it until

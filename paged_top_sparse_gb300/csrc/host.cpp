@@ -41,27 +41,33 @@ inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
 
-// Page-locked staging for the plan-metadata uploads, so that the host->device copy is a
-// plain asynchronous DMA on the caller's stream (a copy from pageable memory makes the GPU
-// wait while the driver stages it).  One ring per process, allocated on first use and never
-// freed; a region is reused only after the event recorded behind its copy has completed.
+// Page-locked staging for the plan-metadata uploads.  The bytes are written into a mapped
+// page-locked ring and a copy kernel on the caller's stream reads them from there: a copy from
+// pageable memory makes the GPU wait while the driver stages it, and a DMA on the copy engine
+// queues behind the caller's own transfers on other streams (for instance the next batch's
+// inputs).  One ring per process, allocated on first use (by the calls that may allocate) and
+// never freed; a region is reused only after the event recorded behind its copy has completed.
 // Uploads that do not fit, uploads into a stream being captured into a graph (the graph must
-// keep reading the plan's own copy), or a failed page-locking copy from pageable memory
-// instead.
+// keep reading the plan's own copy), a failed page-locked allocation or mapping, or a call
+// that may not allocate while the ring does not exist yet copy from pageable memory instead.
 class StagingRing {
  public:
-  cudaError_t upload(void* dst, const void* src, size_t n, cudaStream_t s) {
+  cudaError_t upload(void* dst, const void* src, size_t n, cudaStream_t s, bool may_alloc) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
       (void)cudaGetLastError();
       return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s);
     }
     std::lock_guard<std::mutex> lock(mu_);
-    if (!buf_ && !failed_) {
-      if (cudaHostAlloc(reinterpret_cast<void**>(&buf_), kBytes, cudaHostAllocPortable) !=
-          cudaSuccess) {
+    if (!buf_ && !failed_ && may_alloc) {
+      if (cudaHostAlloc(reinterpret_cast<void**>(&buf_), kBytes,
+                        cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
         buf_ = nullptr;
         failed_ = true;
+        (void)cudaGetLastError();
+      } else if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&dbuf_), buf_, 0) !=
+                 cudaSuccess) {
+        dbuf_ = nullptr;  // not mapped: DMA from the ring instead
         (void)cudaGetLastError();
       }
     }
@@ -76,7 +82,9 @@ class StagingRing {
       if (e != cudaSuccess) return e;
     }
     memcpy(buf_ + off, src, n);
-    cudaError_t e = cudaMemcpyAsync(dst, buf_ + off, n, cudaMemcpyHostToDevice, s);
+    cudaError_t e = (dbuf_ && aligned(dst, 16))
+                        ? launch_staged_copy(dbuf_ + off, dst, n, s)
+                        : cudaMemcpyAsync(dst, buf_ + off, n, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return e;
     cudaEvent_t ev;
     if (!free_ev_.empty()) {
@@ -102,13 +110,13 @@ class StagingRing {
   static bool overlaps(const Live& l, size_t b, size_t e) { return l.begin < e && b < l.end; }
   static constexpr size_t kBytes = 16u << 20;
   std::mutex mu_;
-  uint8_t* buf_ = nullptr;
+  uint8_t* buf_ = nullptr;   // host address of the ring
+  uint8_t* dbuf_ = nullptr;  // its device address (NULL: not mapped)
   bool failed_ = false;
   size_t head_ = 0;
   std::vector<Live> live_;  // in ring order
   std::vector<cudaEvent_t> free_ev_;
 };
-
 StagingRing g_staging;
 
 }  // namespace
@@ -416,7 +424,7 @@ sps_status sps_plan_upload(const sps_plan* pl, void* ws, size_t ws_bytes, sps_st
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   // one copy: zeroed status word and counters, then the plan metadata
-  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s);
+  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s, true);
   if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   return SPS_OK;
 }
@@ -493,11 +501,9 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
     return fail(SPS_EUNSUPPORTED, "sparse_prefill_fwd_fp8qk: needs E4M3 Q, NVFP4 K/V, D = 128");
   DevPlan d = make_dev_plan(pl, ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // counters [1] (forward task cursor), [2] (task count), [3] (inversion buckets scanned) and
-  // [4], [5] (the single-launch inversion's grid barrier) start at zero
-  cudaError_t e = cudaMemsetAsync(d.counters + 1, 0, 5 * sizeof(int32_t), s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
-  e = launch_inversion(d, idx, lse, lse_split_stride, s);
+  // no counter needs clearing here: the inversion writes the task count, and its scan ticket
+  // and grid barrier return to zero when they complete (the plan upload clears them first)
+  cudaError_t e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
   if (kind == FwdKind::kFP8QK)
     return launched(launch_forward_fp8qk(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
@@ -800,7 +806,7 @@ sps_status sps_internal_fwd_noalloc(const sps_plan* pl, const void* q, float q_s
   uint8_t* base = static_cast<uint8_t*>(scratch);
   // the array keeps the previous call's contents: one copy zeroes the status word and
   // counters and writes this plan's metadata over the old one
-  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s);
+  cudaError_t e = g_staging.upload(base, pl->blob.data(), pl->upload_bytes, s, false);
   if (e != cudaSuccess) return cuda_fail(e, "plan metadata -> scratch");
   DevPlan d = make_dev_plan(pl, scratch);
   if (dev_status) d.status = dev_status;

@@ -278,6 +278,8 @@ __global__ void __launch_bounds__(256) scan_kernel(DevPlan p) {
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // every block has taken its ticket: the counter goes back to zero for the next call
+  if (threadIdx.x == 0) p.counters[3] = 0;
   scan_buckets(p, sh);
 }
 
@@ -510,7 +512,8 @@ cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
     else count_kernel<0><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // counters[3] (buckets scanned) was zeroed with the forward's task counters
+  // counters[3] (buckets scanned) is zero: the plan upload clears it and each scan's last block
+  // puts it back to zero
   scan_kernel<<<(unsigned)p.num_buckets, 256, 0, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nblk > 0) {

@@ -47,9 +47,10 @@ struct DevPlan {
   int32_t inv_blocks;       // sum over requests of H_kv * ch_per_bucket
   float sm_scale;
   int32_t* status;
-  int32_t* counters;        // [0] indexer task cursor, [1] forward task cursor, [2] fwd task
-                            // count, [3] inversion buckets scanned, [4] [5] inversion grid
-                            // barrier (arrivals, generation)
+  int32_t* counters;        // [2] fwd task count, [3] inversion buckets scanned, [4] [5]
+                            // inversion grid barrier (arrivals, generation); [0] [1] unused.
+                            // Zeroed by the plan upload; [3] and [4] return to zero when
+                            // their scan / barrier completes
   const int32_t* tok_pos;   // [T]
   const int32_t* tok_req;   // [T]
   const ReqInfo* reqs;      // [batch]
@@ -112,6 +113,10 @@ cudaError_t launch_kv_append(const DevPlan& p, bool nvfp4, const void* knew, con
 cudaError_t launch_quantize_e4m3(const void* in, int64_t n, float scale, void* out,
                                  cudaStream_t st);
 cudaError_t launch_absmax_bf16(const void* in, int64_t n, float* out, cudaStream_t st);
+
+// Copy of n bytes from device-accessible page-locked host memory (src) to device memory (dst),
+// both 16-byte aligned, by a kernel rather than the copy engine.
+cudaError_t launch_staged_copy(const void* src, void* dst, size_t n, cudaStream_t st);
 
 // One-block kernel whose bounded wait on a never-arrived mbarrier must time out.
 cudaError_t launch_wait_timeout(int32_t* status, int64_t limit_ns, cudaStream_t st);
