@@ -8,11 +8,14 @@
 // Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
 // sorted best-first once (bitonic network in registers), so any page of a lower lane is lower
 // than every page of a higher lane.  A selection round is then one warp max-reduction
-// (redux.sync) of the lanes' head keys and one ballot: the lowest lane whose head holds the
-// maximum has the winning page (ties go to the lower page) and shifts its next candidate up.
-// After n_sel - 1 rounds a ballot/popc prefix writes the chosen pages in ascending order.
-// Rows of more than 128 pages first filter their keys down to at most 64 candidates (see
-// topk_filter_kernel) and run the rounds on those.
+// (redux.sync) of the lanes' head keys: the lane whose head holds the maximum takes that page
+// and shifts its next candidate up.  The rounds first run as if no two heads were ever equal
+// (no ballot); the lanes' take counts then sum to n_sel - 1 exactly when no round had a tie,
+// and otherwise the rounds run again with ties going to the lowest such lane (the lower page).
+// The kernel is bound by ALU issue, so the tie-free pass is what most rows pay.  After the
+// rounds a popc prefix writes the chosen pages in ascending order.  Rows of more than 128 pages
+// first filter their keys down to at most 64 candidates (see topk_filter_kernel) and run the
+// rounds on those.
 #include "ptx.cuh"
 #include "sps_internal.h"
 
@@ -47,22 +50,67 @@ __device__ __forceinline__ void sort_best_first(uint32_t (&k)[E], uint32_t (&pg)
       }
 }
 
+// K - 1 selection rounds over the lanes' best-first candidate lists, assuming no two lanes
+// ever show equal heads: the lane whose head equals the warp maximum takes it.  Returns how
+// many of its candidates this lane took; the counts sum to K - 1 exactly when no round had a
+// tie (a tie makes every holder advance), which the caller checks.  `key` is not modified.
+template <int E, int KC>
+__device__ __forceinline__ int rounds_distinct_heads(const uint32_t (&key)[E], int K) {
+  uint32_t h[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) h[j] = key[j];
+  int c = 0;
+#pragma unroll (KC ? KC : 4)
+  for (int round = 1; round < K; ++round) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, h[0]);
+    if (h[0] == m) {
+      ++c;
+#pragma unroll
+      for (int j = 0; j + 1 < E; ++j) h[j] = h[j + 1];
+      h[E - 1] = 0u;
+    }
+  }
+  return c;
+}
+
+// The same rounds with ties resolved: of the lanes whose head equals the maximum, the lowest
+// (it holds the lowest page) takes it.
+template <int E, int KC>
+__device__ __forceinline__ int rounds_lowest_lane(const uint32_t (&key)[E], int K, int lane) {
+  uint32_t h[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) h[j] = key[j];
+  const uint32_t lt = (1u << lane) - 1u;
+  int c = 0;
+#pragma unroll 4
+  for (int round = 1; round < K; ++round) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, h[0]);
+    const uint32_t tie = __ballot_sync(0xffffffffu, h[0] == m);
+    if (h[0] == m && (tie & lt) == 0) {
+      ++c;
+#pragma unroll
+      for (int j = 0; j + 1 < E; ++j) h[j] = h[j + 1];
+      h[E - 1] = 0u;
+    }
+  }
+  return c;
+}
+
 // KC: top_k fixed at compile time (the rounds unroll completely), or 0 for any top_k.
 template <int E, int KC = 0>  // pages per lane: max_pages <= 32 * E
 __global__ void __launch_bounds__(256)
 topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t* __restrict__ idx) {
   const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t R = (int64_t)p.T * p.H;
-  if (r >= R) return;
-  const int o = __ldg(p.tok_pos + r / p.H) >> 7;
+  const uint32_t r = blockIdx.x * 8u + (threadIdx.x >> 5);
+  if (r >= (uint32_t)p.T * (uint32_t)p.H) return;
+  const int o = __ldg(p.tok_pos + r / (uint32_t)p.H) >> 7;
   const int n = o + 1, K = KC ? KC : p.K;
-  int32_t* out = idx + r * K;
+  int32_t* out = idx + (int64_t)r * K;
   if (n <= K) {  // every visible page is kept
     for (int s = lane; s < K; s += 32) out[s] = s < n ? s : -1;
     return;
   }
-  const float* row = scores + r * pitch;
+  const float* row = scores + (int64_t)r * pitch;
   const int base = lane * E;
   uint32_t key[E], pg[E];
 #pragma unroll
@@ -72,19 +120,9 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
     key[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
   }
   sort_best_first<E>(key, pg);
-  const uint32_t lt = (1u << lane) - 1u;
-  int c = 0;  // this lane's candidates taken so far: the first c of the sorted order
-#pragma unroll (KC ? KC : 4)
-  for (int round = 1; round < K; ++round) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-    const uint32_t tie = __ballot_sync(0xffffffffu, key[0] == m);
-    if (key[0] == m && (tie & lt) == 0) {
-      ++c;
-#pragma unroll
-      for (int j = 0; j + 1 < E; ++j) key[j] = key[j + 1];
-      key[E - 1] = 0u;
-    }
-  }
+  int c = rounds_distinct_heads<E, KC>(key, K);
+  if (__reduce_add_sync(0xffffffffu, (uint32_t)c) != (uint32_t)(K - 1))
+    c = rounds_lowest_lane<E, KC>(key, K, lane);
   uint32_t taken = 0;  // bit j: page base + j selected
 #pragma unroll
   for (int j = 0; j < E; ++j)
@@ -104,8 +142,9 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
 }
 
 // Long rows (E >= 8 pages per lane): a filter first.  The (k-1)-th largest of the 32 lane
-// maxima, t0, taken one lane per round, is at most the row's (k-1)-th largest key (those k-1
-// maxima are k-1 distinct keys >= t0), so every page of the answer has key >= t0.  The keys
+// maxima, t0 (read off a bitonic sort of the maxima across the warp), is at most the row's
+// (k-1)-th largest key (those k-1 maxima are k-1 distinct keys >= t0), so every page of the
+// answer has key >= t0.  The keys
 // >= t0 are compacted in page order into two per lane (shared memory, at most 64 of them) and
 // the rounds above run on those; the row's own page, its last visible page, goes last.  A row
 // with more than 64 such keys (heavy ties) runs the rounds on all its keys instead.
@@ -115,17 +154,16 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
                    int32_t* __restrict__ idx) {
   __shared__ uint2 cand[8][64];  // per warp: (key, page) of the compacted candidates
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t r = (int64_t)blockIdx.x * 8 + warp;
-  const int64_t R = (int64_t)p.T * p.H;
-  if (r >= R) return;
-  const int o = __ldg(p.tok_pos + r / p.H) >> 7;
+  const uint32_t r = blockIdx.x * 8u + warp;
+  if (r >= (uint32_t)p.T * (uint32_t)p.H) return;
+  const int o = __ldg(p.tok_pos + r / (uint32_t)p.H) >> 7;
   const int n = o + 1, K = p.K;
-  int32_t* out = idx + r * K;
+  int32_t* out = idx + (int64_t)r * K;
   if (n <= K) {  // every visible page is kept
     for (int s = lane; s < K; s += 32) out[s] = s < n ? s : -1;
     return;
   }
-  const float* row = scores + r * pitch;
+  const float* row = scores + (int64_t)r * pitch;
   const int base = lane * E;
   uint32_t key[E];
   uint32_t lm = 0;  // the lane's largest key
@@ -135,20 +173,24 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
     key[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
     lm = max(lm, key[j]);
   }
-  // t0: the (K-1)-th largest lane maximum (0 when fewer lanes hold candidates)
-  uint32_t t0 = 0, v = lm;
-  for (int round = 1; round < K; ++round) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, v);
-    t0 = m;
-    if (m == 0u) break;
-    const uint32_t tie = __ballot_sync(0xffffffffu, v == m);
-    if (lane == __ffs(tie) - 1) v = 0u;
-  }
+  // t0: the (K-1)-th largest lane maximum (0 when fewer lanes hold candidates), from a
+  // bitonic sort of the 32 lane maxima into descending lane order
+  uint32_t v = lm;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t w = __shfl_xor_sync(0xffffffffu, v, stride);
+      // descending runs where bit `size` of the lane is 0; the lower lane of a pair keeps
+      // the larger key in a descending run
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? max(v, w) : min(v, w);
+    }
+  const uint32_t t0 = K - 2 < 32 ? __shfl_sync(0xffffffffu, v, K - 2) : 0u;
   int cnt = 0;
 #pragma unroll
   for (int j = 0; j < E; ++j) cnt += (key[j] != 0u && key[j] >= t0) ? 1 : 0;
   const int total = __reduce_add_sync(0xffffffffu, cnt);
-  const uint32_t lt = (1u << lane) - 1u;
   if (total <= 64) {
     int pos = cnt;
 #pragma unroll
@@ -171,17 +213,9 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
     const uint32_t page0 = 2 * lane < total ? cand[warp][2 * lane].y : 0u;
     const uint32_t page1 = 2 * lane + 1 < total ? cand[warp][2 * lane + 1].y : 0u;
     sort_best_first<2>(ck, cp);
-    int c = 0;
-#pragma unroll 4
-    for (int round = 1; round < K; ++round) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, ck[0]);
-      const uint32_t tie = __ballot_sync(0xffffffffu, ck[0] == m);
-      if (ck[0] == m && (tie & lt) == 0) {
-        ++c;
-        ck[0] = ck[1];
-        ck[1] = 0u;
-      }
-    }
+    int c = rounds_distinct_heads<2, 0>(ck, K);
+    if (__reduce_add_sync(0xffffffffu, (uint32_t)c) != (uint32_t)(K - 1))
+      c = rounds_lowest_lane<2, 0>(ck, K, lane);
     uint32_t taken = 0;  // bit j: compacted candidate 2 lane + j selected
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -203,18 +237,7 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
 #pragma unroll
   for (int j = 0; j < E; ++j) pg[j] = (uint32_t)j;
   sort_best_first<E>(key, pg);
-  int c = 0;
-#pragma unroll 4
-  for (int round = 1; round < K; ++round) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-    const uint32_t tie = __ballot_sync(0xffffffffu, key[0] == m);
-    if (key[0] == m && (tie & lt) == 0) {
-      ++c;
-#pragma unroll
-      for (int j = 0; j + 1 < E; ++j) key[j] = key[j + 1];
-      key[E - 1] = 0u;
-    }
-  }
+  const int c = rounds_lowest_lane<E, 0>(key, K, lane);
   uint32_t taken = 0;
 #pragma unroll
   for (int j = 0; j < E; ++j)

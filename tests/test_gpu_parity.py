@@ -236,8 +236,6 @@ def test_determinism_three_runs():
         run = DeviceRun(w, t)
         run.run_all()
         outs.append([x.cpu().clone() for x in (run.scores, run.idx, run.partial, run.lse, run.out)])
-    for a, b in zip(outs[0], outs[1] + outs[2]):
-        pass
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
             assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
@@ -595,3 +593,79 @@ def test_inversion_when_the_single_launch_does_not_fit():
     ent = run.ws_array(info.off_entries, 2 * len(er), np.int32).reshape(-1, 2)
     assert np.array_equal(ent[:, 0], er)
     assert np.array_equal(ent[:, 1] & 63, es)
+
+
+@pytest.mark.parametrize("q_len", [300, 12000])
+def test_repeated_forward_after_one_upload(q_len):
+    """Three forward calls on one uploaded workspace give bit-identical partials, LSEs and
+    outputs: the inversion's scan ticket and grid barrier return to zero after each call, so no
+    call clears counters.  300 tokens take the single cooperative inversion launch, 12000 tokens
+    x 32 heads the three-kernel path."""
+    from tests.gpu_helpers import DeviceRun
+
+    w = synth.workload("custom", seed=32, q_lens=[q_len], ctx_lens=[200], num_q_heads=32,
+                       num_kv_heads=2, head_dim=128, top_k=16)
+    run = DeviceRun(w, synth.make_tensors(w))
+    run.indexer()
+    run.topk()
+    ref = None
+    for _ in range(3):
+        run.partial.fill_(float("nan"))
+        run.lse.fill_(float("nan"))
+        run.forward()
+        run.combine()
+        torch.cuda.synchronize()
+        assert run.status() == 0
+        got = [run.partial.view(torch.int32).clone(), run.lse.view(torch.int32).clone(),
+               run.out.view(torch.int16).clone()]
+        if ref is None:
+            ref = got
+        else:
+            for a, b in zip(ref, got):
+                assert torch.equal(a, b)
+    idx_all = run.idx.cpu().numpy()
+    offsets, er, es = orc.inversion(oracle_problem(w), idx_all)
+    info = run.plan.info()
+    got_off = run.ws_array(info.off_bucket_offsets, len(offsets), np.int32)
+    assert np.array_equal(got_off, offsets.astype(np.int32))
+    ent = run.ws_array(info.off_entries, 2 * len(er), np.int32).reshape(-1, 2)
+    assert np.array_equal(ent[:, 0], er)
+
+
+def test_plan_upload_does_not_wait_for_other_streams_copies():
+    """The plan upload is a kernel reading the library's mapped page-locked ring, so it does not
+    queue behind a large host-to-device copy running on another stream; the uploaded plan is
+    the one the next calls use."""
+    from paged_top_sparse_gb300 import binding as B
+    from tests.gpu_helpers import DeviceRun
+
+    w = _workload("ragged")
+    run = DeviceRun(w, synth.make_tensors(w))
+    run.run_all()
+    ref = run.out.view(torch.int16).clone()
+
+    big_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(1 << 30, dtype=torch.uint8, device="cuda:0")
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    ev[0].record(main)
+    side.wait_event(ev[0])
+    with torch.cuda.stream(side):
+        big_d.copy_(big_h, non_blocking=True)
+    ev[2].record(side)
+    run.ws.zero_()
+    B.sps_plan_upload(run.plan, run.ws)
+    ev[1].record(main)
+    run.out.zero_()
+    run.indexer()
+    run.topk()
+    run.forward()
+    run.combine()
+    torch.cuda.synchronize()
+    assert run.status() == 0
+    assert torch.equal(run.out.view(torch.int16), ref)
+    upload_ms, copy_ms = ev[0].elapsed_time(ev[1]), ev[0].elapsed_time(ev[2])
+    assert copy_ms > 1.0  # 1 GiB over the host link takes milliseconds
+    assert upload_ms < 0.5 * copy_ms, (upload_ms, copy_ms)
