@@ -14,7 +14,8 @@
 // and otherwise the rounds run again with ties going to the lowest such lane (the lower page).
 // The kernel is bound by ALU issue, so the tie-free pass is what most rows pay.  After the
 // rounds a popc prefix writes the chosen pages in ascending order.  Rows of more than 128 pages
-// first filter their keys down to at most 64 candidates (see topk_filter_kernel) and run the
+// first filter their keys down to at most 64 candidates (see topk_filter_kernel: pages dealt
+// to the lanes round-robin, so that every lane is busy and loads are contiguous) and run the
 // rounds on those.
 #include "ptx.cuh"
 #include "sps_internal.h"
@@ -141,20 +142,22 @@ topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t*
     if ((taken >> j) & 1u) out[before++] = base + j;
 }
 
-// Long rows (E >= 8 pages per lane): a filter first.  The (k-1)-th largest of the 32 lane
-// maxima, t0 (read off a bitonic sort of the maxima across the warp), is at most the row's
-// (k-1)-th largest key (those k-1 maxima are k-1 distinct keys >= t0), so every page of the
-// answer has key >= t0.  The keys
-// >= t0 are compacted in page order into two per lane (shared memory, at most 64 of them) and
-// the rounds above run on those; the row's own page, its last visible page, goes last.  A row
-// with more than 64 such keys (heavy ties) runs the rounds on all its keys instead.
-template <int E>
+// Long rows: a filter first.  Lane l holds the pages l, l + 32, l + 64, ... (E of them), so
+// every lane has work and each load instruction reads 128 contiguous bytes.  The (k-1)-th
+// largest of the 32 lane maxima, t0 (read off a bitonic sort of the maxima across the warp), is
+// at most the row's (k-1)-th largest key (those k-1 maxima are k-1 distinct keys >= t0), so
+// every page of the answer has key >= t0.  The keys >= t0 are compacted in page order (one
+// ballot per stride of 32 pages) into two per lane (shared memory, at most 64 of them) and the
+// rounds above run on those; the row's own page, its last visible page, goes last.  A row with
+// more than 64 such keys (heavy ties) reloads its keys with EH adjacent pages per lane and runs
+// the rounds on all of them.
+template <int E, int EH>  // E * 32 >= max_pages, EH * 32 >= max_pages (EH a power of two)
 __global__ void __launch_bounds__(256)
 topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
                    int32_t* __restrict__ idx) {
   __shared__ uint2 cand[8][64];  // per warp: (key, page) of the compacted candidates
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t r = blockIdx.x * 8u + warp;
+  const uint32_t r = blockIdx.x * 8u + warp;  // rows x top_k < 2^31
   if (r >= (uint32_t)p.T * (uint32_t)p.H) return;
   const int o = __ldg(p.tok_pos + r / (uint32_t)p.H) >> 7;
   const int n = o + 1, K = p.K;
@@ -164,12 +167,11 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
     return;
   }
   const float* row = scores + (int64_t)r * pitch;
-  const int base = lane * E;
   uint32_t key[E];
   uint32_t lm = 0;  // the lane's largest key
 #pragma unroll
   for (int j = 0; j < E; ++j) {
-    const int page = base + j;
+    const int page = j * 32 + lane;
     key[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
     lm = max(lm, key[j]);
   }
@@ -187,21 +189,18 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
       v = keep_max ? max(v, w) : min(v, w);
     }
   const uint32_t t0 = K - 2 < 32 ? __shfl_sync(0xffffffffu, v, K - 2) : 0u;
-  int cnt = 0;
+  // compaction in page order: stride j holds the pages 32 j .. 32 j + 31, lane order
+  const uint32_t lt = (1u << lane) - 1u;
+  int total = 0;  // warp-uniform
 #pragma unroll
-  for (int j = 0; j < E; ++j) cnt += (key[j] != 0u && key[j] >= t0) ? 1 : 0;
-  const int total = __reduce_add_sync(0xffffffffu, cnt);
+  for (int j = 0; j < E; ++j) {
+    const bool keep = key[j] != 0u && key[j] >= t0;
+    const uint32_t b = __ballot_sync(0xffffffffu, keep);
+    const int at = total + __popc(b & lt);
+    if (keep && at < 64) cand[warp][at] = make_uint2(key[j], (uint32_t)(j * 32 + lane));
+    total += __popc(b);
+  }
   if (total <= 64) {
-    int pos = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, pos, d);
-      if (lane >= d) pos += y;
-    }
-    pos -= cnt;
-#pragma unroll
-    for (int j = 0; j < E; ++j)
-      if (key[j] != 0u && key[j] >= t0) cand[warp][pos++] = make_uint2(key[j], (uint32_t)(base + j));
     __syncwarp();
     uint32_t ck[2], cp[2];
 #pragma unroll
@@ -232,17 +231,22 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
     if (lane == 0) out[K - 1] = o;  // the own page is the row's last visible page
     return;
   }
-  // heavy ties: the rounds on every key of the row
-  uint32_t pg[E];
+  // heavy ties: the rounds on every key of the row, EH adjacent pages per lane
+  const int base = lane * EH;
+  uint32_t hk[EH], pg[EH];
 #pragma unroll
-  for (int j = 0; j < E; ++j) pg[j] = (uint32_t)j;
-  sort_best_first<E>(key, pg);
-  const int c = rounds_lowest_lane<E, 0>(key, K, lane);
+  for (int j = 0; j < EH; ++j) {
+    const int page = base + j;
+    hk[j] = (page < n && page != o) ? score_key(__ldg(row + page)) : 0u;
+    pg[j] = (uint32_t)j;
+  }
+  sort_best_first<EH>(hk, pg);
+  const int c = rounds_lowest_lane<EH, 0>(hk, K, lane);
   uint32_t taken = 0;
 #pragma unroll
-  for (int j = 0; j < E; ++j)
+  for (int j = 0; j < EH; ++j)
     if (j < c) taken |= 1u << pg[j];
-  if (o / E == lane) taken |= 1u << (o % E);
+  if (o / EH == lane) taken |= 1u << (o % EH);
   int before = __popc(taken);
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -251,7 +255,7 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
   }
   before -= __popc(taken);
 #pragma unroll
-  for (int j = 0; j < E; ++j)
+  for (int j = 0; j < EH; ++j)
     if ((taken >> j) & 1u) out[before++] = base + j;
 }
 
@@ -275,9 +279,13 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
     if (k16) topk_kernel<4, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
     else topk_kernel<4><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   } else if (p.max_pages <= 256) {
-    topk_filter_kernel<8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    topk_filter_kernel<8, 8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else if (p.max_pages <= 320) {
+    topk_filter_kernel<10, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+  } else if (p.max_pages <= 384) {
+    topk_filter_kernel<12, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   } else {
-    topk_filter_kernel<16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    topk_filter_kernel<16, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
   }
   return cudaGetLastError();
 }

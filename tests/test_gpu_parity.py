@@ -152,6 +152,9 @@ def test_topk_bit_exact_on_shared_scores(name):
     ([64], [20000], 16),          # 157 pages
     ([200], [3000], 32),          # 25 pages, k above the page count for most rows
     ([130], [38000], 64),         # 298 pages, the largest k
+    ([300], [40000], 16),         # 315 pages
+    ([100], [44000], 16),         # 345 pages
+    ([50], [65000], 16),          # 508 pages
 ])
 def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     """Scores drawn from {-1.5, ..., 1.5} with signed zeros: most pages tie with others, so
