@@ -77,7 +77,9 @@ combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
     // ---------------- producer warp
     uint32_t slot = 0, phase = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int64_t r0 = tile * TR;
+      // tiles from the last rows down: a page-parallel forward writes the highest pages last,
+      // and only late rows select those, so the first tiles read partials still in L2
+      const int64_t r0 = (ntiles - 1 - tile) * TR;
       const int nvalid = (int)((rows - r0) < TR ? (rows - r0) : TR);
       constexpr int RPL = TR / 32;  // rows per lane: 1 or 2
       float m[RPL];
@@ -151,7 +153,7 @@ combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
     const int rsub = lane / LPR;        // row within an instruction
     const int c4 = lane % LPR;          // 16-byte column group
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int64_t r0 = tile * TR;
+      const int64_t r0 = (ntiles - 1 - tile) * TR;  // same order as the producer
       float acc[IT][EPL];
       float wsum[IT];
 #pragma unroll
