@@ -49,3 +49,23 @@ def test_single_rank_is_identity():
 
     assert bench.max_over_ranks([1.5, 2.5], 1) == [1.5, 2.5]
     assert bench.job_tokens_per_s(8192, 1, 1.0) == pytest.approx(8192e3)
+
+
+def test_e2e_input_slices_cover_every_byte():
+    """The end-to-end loop cuts each (device, host) input pair into byte slices dealt over the
+    H2D streams; copying every slice must reproduce each tensor exactly."""
+    import bench
+
+    torch = pytest.importorskip("torch")
+    g = torch.Generator().manual_seed(3)
+    hosts = [torch.randn(1000, 37, generator=g), torch.arange(12345, dtype=torch.int16),
+             torch.randint(0, 255, (3, 5, 7), generator=g, dtype=torch.uint8)]
+    devs = [torch.empty_like(h) for h in hosts]
+    sl = bench._byte_chunks(list(zip(devs, hosts)), chunk_bytes=4096)
+    assert all(d.numel() == h.numel() <= 4096 for d, h in sl)
+    assert sum(h.numel() for _, h in sl) == sum(h.numel() * h.element_size() for h in hosts)
+    for j in range(3):  # three streams' shares, in any order
+        for d, h in sl[j::3]:
+            d.copy_(h)
+    for d, h in zip(devs, hosts):
+        assert torch.equal(d, h)
