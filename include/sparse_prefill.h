@@ -176,8 +176,9 @@ sps_status indexer_scores(const sps_plan* plan, const void* q_idx, float q_scale
                           void* workspace, sps_stream_t stream);
 
 /*
- * topk_select -- step 2 (north-star definition; bitwise-stable selection, "MSA PR 36",
- * Kernel performance table: top-k bitwise identical).
+ * topk_select -- step 2 (the method's page selection, with the row's own page -- the one page
+ * "MSA PR 21", K1 Softmax, masks causally -- always kept; bitwise-stable selection, "MSA PR
+ * 36", Kernel performance table: top-k bitwise identical).
  *   scores  device FP32 [T*H][score_pitch] as written by indexer_scores (entries p <= o read)
  *   idx     device int32 [T*H][top_k] out: the selected pages of each row in ascending page
  *           order, padded with -1 when the row sees fewer than top_k pages.

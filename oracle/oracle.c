@@ -14,8 +14,9 @@
  *                    score buffer [total_q * num_heads, >= max_pages] with a row pitch.)
  *   top-k            the own page is always kept; the other min(k, o+1) - 1 pages are the
  *                    best by (score descending, page ascending); emitted as an ascending
- *                    set, padded with -1.  (north-star definition; "MSA PR 36", Validation:
- *                    bitwise-stable top-k.)
+ *                    set, padded with -1.  (the method's page selection; the own page is the
+ *                    one page "MSA PR 21", K1 Softmax, masks causally; "MSA PR 36",
+ *                    Validation: bitwise-stable top-k.)
  *   inversion        for every (request, logical page, kv head) bucket, the ordered list of
  *                    (row, slot) pairs that selected it, rows ascending.
  *   forward          per (row, slot): softmax over the visible keys of the selected page,

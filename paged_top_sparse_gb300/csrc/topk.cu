@@ -1,7 +1,9 @@
 // topk.cu -- per-row top-k page selection, one warp per row.
 //
-// Contract (north-star definition of the method; "MSA PR 36: Q8KV8 prefill indexer" relies on
-// a bitwise-stable selection): the row's own page o is always kept; the other
+// Contract (the method's page selection: every row attends its own page, the one page the
+// forward of "MSA PR 21: Q8KV4 paged sparse prefill", K1 Softmax, masks causally; "MSA PR 36:
+// Q8KV8 prefill indexer", Kernel performance, relies on a bitwise-stable selection): the row's
+// own page o is always kept; the other
 // n_sel - 1 = min(k, o+1) - 1 pages are the best by (score descending, page ascending), with
 // -0.0 equal to +0.0; output in ascending page order, padded with -1.
 //
