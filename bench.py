@@ -356,18 +356,21 @@ def run_gpu(args, rank, world):
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     scores = torch.empty((R, w.max_pages), dtype=torch.float32, device=dev)
     idx = torch.empty((R, K), dtype=torch.int32, device=dev)
-    bf16p = args.partials == "bf16"
-    partial = torch.empty((K, R, D), dtype=torch.bfloat16 if bf16p else torch.float32, device=dev)
+    bf16p = args.partials != "fp32"  # 16-bit partial storage (BF16 or FP16)
+    pdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.partials]
+    partial = torch.empty((K, R, D), dtype=pdt, device=dev)
     lse = torch.empty((K, R), dtype=torch.float32, device=dev)
     out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    fwd_call = B.sparse_prefill_fwd_bf16 if bf16p else B.sparse_prefill_fwd
+    fwd_call = {"fp32": B.sparse_prefill_fwd, "bf16": B.sparse_prefill_fwd_bf16,
+                "f16": B.sparse_prefill_fwd_f16}[args.partials]
     if args.fp8qk:
         if bf16p or w.kv_dtype != "nvfp4":
             raise SystemExit("--fp8qk needs the quantised workload (prefill8k_q) and FP32 partials")
         fwd_call = B.sparse_prefill_fwd_fp8qk
-    combine_call = B.partial_combine_bf16 if bf16p else B.partial_combine
+    combine_call = {"fp32": B.partial_combine, "bf16": B.partial_combine_bf16,
+                    "f16": B.partial_combine_f16}[args.partials]
 
     def step(ev, di=din, out_=out):
         pl = B.Plan(*plan_args, **plan_kw)
@@ -465,9 +468,10 @@ def run_gpu(args, rank, world):
         "dtype": "fp16" if w.kv_dtype == "nvfp4" else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, quantised where the workload says; permuted "
                 "page table)",
-        "config": {"workload": _describe(w, args.workload) + (", BF16 partials" if bf16p else "")
+        "config": {"workload": _describe(w, args.workload)
+                               + ({"bf16": ", BF16 partials", "f16": ", FP16 partials"}.get(args.partials, ""))
                                + (", FP8 Q K^T on E4M3-rounded K" if args.fp8qk else ""),
-                   "partials": "bf16" if bf16p else "fp32",
+                   "partials": args.partials,
                    "batch": int(w.batch), "seq_len": int(max(w.q_lens)), "rows": int(R),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (256 MB write); per-step CUDA events"},
@@ -723,9 +727,10 @@ def main():
     ap.add_argument("--fp8qk", action="store_true",
                     help="quantised workload only: the pages' Q8KV4 route (K rounded to E4M3, "
                          "FP8 Q K^T) through sparse_prefill_fwd_fp8qk")
-    ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
-                    help="partial storage: fp32 (the contract; default) or bf16 (the pages' "
-                         "storage, sparse_prefill_fwd_bf16 + partial_combine_bf16)")
+    ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16", "f16"],
+                    help="partial storage: fp32 (the contract; default), or the pages' 16-bit "
+                         "storage, bf16 or f16 (sparse_prefill_fwd_{bf16,f16} + "
+                         "partial_combine_{bf16,f16})")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))

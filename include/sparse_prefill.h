@@ -257,6 +257,29 @@ sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
                                 float* out_lse, int32_t* dev_status, sps_stream_t stream);
 
 /*
+ * sparse_prefill_fwd_f16 / partial_combine_f16 -- the same two steps with the partial outputs
+ * stored as FP16, the other 16-bit storage the pages name ("MSA PR 21", Combine: keep
+ * BF16/FP16 partials).  FP16 carries 11 significant bits against BF16's 8, so its rounding
+ * adds far less to the output error; its range is that of the FP16 V operand the forward
+ * already uses (|v| < 65504), which bounds every partial, a convex combination of V rows.
+ *   partial_f16  device FP16; element (s, r, d) at partial_f16[s * split_stride + r * D + d]
+ *                (elements); 16-byte aligned, split_stride a multiple of 8 and >= rows * D
+ * Every other argument, the LSE and the output are those of sparse_prefill_fwd and
+ * partial_combine.  The forward rounds each normalised partial to FP16 (nearest even); the
+ * combine widens them exactly to FP32 and accumulates in FP32.
+ */
+sps_status sparse_prefill_fwd_f16(const sps_plan* plan, const void* q, float q_scale,
+                                  const void* k_cache, const void* v_cache, const void* k_scales,
+                                  const void* v_scales, const int32_t* page_table,
+                                  const int32_t* idx, void* partial_f16, int64_t split_stride,
+                                  float* lse, int64_t lse_split_stride, void* workspace,
+                                  sps_stream_t stream);
+sps_status partial_combine_f16(int64_t rows, int32_t splits, int32_t head_dim,
+                               const void* partial_f16, int64_t split_stride, const float* lse,
+                               int64_t lse_split_stride, void* out_bf16, int64_t out_row_stride,
+                               float* out_lse, int32_t* dev_status, sps_stream_t stream);
+
+/*
  * sparse_prefill_fwd_fp8qk -- the pages' own Q8KV4 route ("MSA PR 21: Q8KV4 paged sparse
  * prefill": QMUL4 dequant, whose only rounding is the final conversion of the code x scale
  * product to E4M3, and FP8 UMMA for Q K^T): the same arguments and outputs as

@@ -87,10 +87,12 @@ def lib(path: str | None = None):
     L.partial_combine.argtypes = [i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, vp, vp]
     L.sparse_prefill_fwd_bf16.argtypes = L.sparse_prefill_fwd.argtypes
     L.sparse_prefill_fwd_fp8qk.argtypes = L.sparse_prefill_fwd.argtypes
+    L.sparse_prefill_fwd_f16.argtypes = L.sparse_prefill_fwd.argtypes
     L.sps_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.sps_quantize_e4m3.argtypes = [vp, i64, f32, vp, vp]
     L.sps_absmax_bf16.argtypes = [vp, i64, vp, vp]
     L.partial_combine_bf16.argtypes = L.partial_combine.argtypes
+    L.partial_combine_f16.argtypes = L.partial_combine.argtypes
     L.sparse_prefill_fwd_noalloc.argtypes = [vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i64,
                                              vp, vp]
     L.sps_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
@@ -199,6 +201,16 @@ def sparse_prefill_fwd_bf16(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, 
                                          _ptr(workspace), _stream(stream)))
 
 
+def sparse_prefill_fwd_f16(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
+                           page_table, idx, partial, lse, workspace, stream=None):
+    """As ``sparse_prefill_fwd`` with ``partial`` an FP16 [splits][rows][D] view."""
+    _check(lib().sparse_prefill_fwd_f16(plan.handle, _ptr(q), float(q_scale), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                        _ptr(page_table), _ptr(idx), _ptr(partial),
+                                        partial.stride(0), _ptr(lse), lse.stride(0),
+                                        _ptr(workspace), _stream(stream)))
+
+
 def sparse_prefill_fwd_fp8qk(plan: Plan, q, q_scale, k_cache, v_cache, k_scales, v_scales,
                              page_table, idx, partial, lse, workspace, stream=None):
     """As ``sparse_prefill_fwd``: E4M3 Q, NVFP4 K rounded to E4M3, FP8 Q K^T (the pages' route)."""
@@ -233,6 +245,14 @@ def partial_combine_bf16(partial, lse, out, out_lse=None, dev_status=None, strea
     _check(lib().partial_combine_bf16(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
                                       lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
                                       _ptr(dev_status), _stream(stream)))
+
+
+def partial_combine_f16(partial, lse, out, out_lse=None, dev_status=None, stream=None):
+    """As ``partial_combine`` with ``partial`` FP16 [splits][rows][D] (rows contiguous)."""
+    S, R, D = partial.shape
+    _check(lib().partial_combine_f16(R, S, D, _ptr(partial), partial.stride(0), _ptr(lse),
+                                     lse.stride(0), _ptr(out), out.stride(0), _ptr(out_lse),
+                                     _ptr(dev_status), _stream(stream)))
 
 
 def sps_kv_append(plan: Plan, k_new, v_new, page_table, k_cache, v_cache, k_scales, v_scales,

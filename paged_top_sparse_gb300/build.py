@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsps.so")
 SOURCES = ["host.cpp", "combine.cu", "topk.cu", "inversion.cu", "indexer.cu", "forward.cu",
-           "noalloc.cu", "dequant.cu", "selftest.cu", "kvappend.cu", "upload.cu"]
+           "forward_p16.cu", "noalloc.cu", "dequant.cu", "selftest.cu", "kvappend.cu", "upload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -14,6 +14,9 @@
 // BF16 partial values) of a few rows, so shared-memory reads are conflict-free and the BF16
 // output of a row is one contiguous warp store.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "sps_internal.h"
@@ -42,7 +45,7 @@ struct __align__(128) CombineSmem {
   int abort_flag;
 };
 
-// P: partial element type, float or __nv_bfloat16.
+// P: partial element type, float, __nv_bfloat16 or __half.
 template <int D, typename P>
 __global__ void __launch_bounds__(kThreads, 3)
 combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
@@ -181,8 +184,15 @@ combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
             float v[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
-              if (PE == 4) v[e] = __uint_as_float(wd[e]);
-              else v[e] = __uint_as_float(e & 1 ? wd[e / 2] & 0xffff0000u : wd[e / 2] << 16);
+              if (PE == 4) {
+                v[e] = __uint_as_float(wd[e]);
+              } else if (std::is_same<P, __half>::value) {
+                const uint32_t hw = wd[e / 2];
+                const __half2 h2 = *reinterpret_cast<const __half2*>(&hw);
+                v[e] = e & 1 ? __high2float(h2) : __low2float(h2);
+              } else {
+                v[e] = __uint_as_float(e & 1 ? wd[e / 2] & 0xffff0000u : wd[e / 2] << 16);
+              }
             }
             const bool use = w != 0.f;
 #pragma unroll
@@ -268,6 +278,15 @@ cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const 
                                          static_cast<const __nv_bfloat16*>(partial), split_stride,
                                          lse, lse_split_stride, out, out_row_stride, out_lse,
                                          status, st);
+}
+
+cudaError_t launch_combine_f16p(int64_t rows, int32_t splits, int32_t D, const void* partial,
+                                int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                                void* out, int64_t out_row_stride, float* out_lse,
+                                int32_t* status, cudaStream_t st) {
+  return launch_combine_t<__half>(rows, splits, D, static_cast<const __half*>(partial),
+                                  split_stride, lse, lse_split_stride, out, out_row_stride,
+                                  out_lse, status, st);
 }
 
 }  // namespace sps

@@ -16,26 +16,6 @@
 
 namespace sps {
 
-// Two E4M3 codes (low byte = first element) -> f16x2 (low half = first element).
-__device__ __forceinline__ uint32_t cvt_e4m3x2(uint16_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
-  return r;
-}
-// Two E2M1 codes in one byte (low nibble = first element) -> f16x2.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(uint16_t byte_in_low) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tmov.b16 {t, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "h"(byte_in_low));
-  return r;
-}
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 x = *reinterpret_cast<__half2*>(&a), y = *reinterpret_cast<__half2*>(&b);
-  __half2 z = __hmul2(x, y);
-  return *reinterpret_cast<uint32_t*>(&z);
-}
-
 namespace {
 
 __global__ void __launch_bounds__(256)

@@ -132,7 +132,7 @@ struct sps_plan {
   // workspace layout (bytes)
   int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
           off_page_req = 0, off_idx_tasks = 0, off_chunk_offsets = 0, off_bucket_totals = 0,
-          off_qconv = -1, off_kconv = -1, off_vconv = -1,
+          off_qconv = -1, off_kconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
   int64_t upload_bytes = 0;  // [0, upload_bytes) of the workspace comes from `blob`
   std::vector<uint8_t> blob;
@@ -306,14 +306,15 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
-  // FP16 staging of quantised inputs for the tensor-core paths (E4M3 x E4M3 indexing runs on
-  // the FP8 tensor core directly and needs none)
+  // FP16 staging of quantised inputs for the tensor-core paths: an exact FP16 copy of E4M3 Q;
+  // the indexer with NVFP4 keys also takes an FP16 copy of the key cache.  The forward
+  // dequantises NVFP4 K/V inside its loader and needs no copy of the caches.  (E4M3 x E4M3
+  // indexing runs on the FP8 tensor core directly and needs none.)
   const bool idx_fp16 = p.idx_k_dtype == SPS_NVFP4;
   const int64_t cache_elems = (int64_t)p.num_phys_pages * p.num_kv_heads * kPage * p.head_dim;
   if (p.q_dtype == SPS_E4M3 || (idx_fp16 && p.idx_q_dtype == SPS_E4M3))
     pl->off_qconv = take(2 * pl->R * p.head_dim);
-  if (p.kv_dtype == SPS_NVFP4 || idx_fp16) pl->off_kconv = take(2 * cache_elems);
-  if (p.kv_dtype == SPS_NVFP4) pl->off_vconv = take(2 * cache_elems);
+  if (idx_fp16) pl->off_kconv = take(2 * cache_elems);
   pl->ws_bytes = off;
 
   // the host image of [0, upload_end): the status word and counters (zero), then the metadata
@@ -392,7 +393,6 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
   d.qconv = pl->off_qconv >= 0 ? base + pl->off_qconv : nullptr;
   d.kconv = pl->off_kconv >= 0 ? base + pl->off_kconv : nullptr;
-  d.vconv = pl->off_vconv >= 0 ? base + pl->off_vconv : nullptr;
   return d;
 }
 
@@ -471,14 +471,15 @@ sps_status topk_select(const sps_plan* pl, const float* scores, int64_t score_pi
 
 namespace {
 
-// The forward with FP32 or BF16 partials, or the FP8-QK route: the same checks and launches.
-enum class FwdKind { kFP32, kBF16Partials, kFP8QK };
+// The forward with FP32, BF16 or FP16 partials, or the FP8-QK route: the same checks and
+// launches.
+enum class FwdKind { kFP32, kBF16Partials, kF16Partials, kFP8QK };
 sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const void* k_cache,
                       const void* v_cache, const void* k_scales, const void* v_scales,
                       const int32_t* page_table, const int32_t* idx, void* partial,
                       int64_t split_stride, float* lse, int64_t lse_split_stride, void* ws,
                       sps_stream_t stream, FwdKind kind) {
-  const bool bf16p = kind == FwdKind::kBF16Partials;
+  const bool p16 = kind == FwdKind::kBF16Partials || kind == FwdKind::kF16Partials;
   sps_status st = check_plan_ws(pl, ws);
   if (st != SPS_OK) return st;
   const sps_problem& p = pl->pb;
@@ -490,7 +491,7 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
       (k_scales && !aligned(k_scales, 16)) || (v_scales && !aligned(v_scales, 16)))
     return fail(SPS_EINVAL, "sparse_prefill_fwd: q/k/v buffers must be 16-byte aligned");
   if (!aligned(partial, 16)) return fail(SPS_EINVAL, "partial must be 16-byte aligned");
-  const int64_t qa = bf16p ? 8 : 4;  // elements per 16 bytes
+  const int64_t qa = p16 ? 8 : 4;  // elements per 16 bytes
   if (split_stride < pl->R * p.head_dim || split_stride % qa)
     return fail(SPS_EINVAL, "split_stride must be >= rows*head_dim and a multiple of %lld",
                 (long long)qa);
@@ -511,10 +512,15 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
                                          static_cast<float*>(partial), split_stride, lse,
                                          lse_split_stride, s),
                     "forward launch");
-  if (bf16p)
+  if (kind == FwdKind::kBF16Partials)
     return launched(launch_forward_bf16p(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
                                          k_scales, v_scales, page_table, partial, split_stride,
                                          lse, lse_split_stride, s),
+                    "forward launch");
+  if (kind == FwdKind::kF16Partials)
+    return launched(launch_forward_f16p(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache,
+                                        k_scales, v_scales, page_table, partial, split_stride,
+                                        lse, lse_split_stride, s),
                     "forward launch");
   return launched(launch_forward(d, p.q_dtype, p.kv_dtype, q, q_scale, k_cache, v_cache, k_scales,
                                  v_scales, page_table, static_cast<float*>(partial),
@@ -525,7 +531,8 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
 sps_status combine_common(int64_t rows, int32_t splits, int32_t head_dim, const void* partial,
                           int64_t split_stride, const float* lse, int64_t lse_split_stride,
                           void* out_bf16, int64_t out_row_stride, float* out_lse,
-                          int32_t* dev_status, sps_stream_t stream, bool bf16p) {
+                          int32_t* dev_status, sps_stream_t stream, int ptype) {
+  const bool p16 = ptype != 0;  // 0: FP32, 1: BF16, 2: FP16 partials
   if (rows < 0) return fail(SPS_EINVAL, "rows must be >= 0");
   if (splits < 1 || splits > kMaxTopK) return fail(SPS_EINVAL, "splits must be in [1, 64]");
   if (head_dim != 64 && head_dim != 128) return fail(SPS_EUNSUPPORTED, "head_dim must be 64 or 128");
@@ -533,7 +540,7 @@ sps_status combine_common(int64_t rows, int32_t splits, int32_t head_dim, const 
   if (!partial || !lse || !out_bf16) return fail(SPS_EINVAL, "partial_combine: NULL pointer");
   if (!aligned(partial, 16) || !aligned(out_bf16, 16) || !aligned(lse, 4))
     return fail(SPS_EINVAL, "partial/out must be 16-byte aligned, lse 4-byte aligned");
-  const int64_t qa = bf16p ? 8 : 4;  // elements per 16 bytes
+  const int64_t qa = p16 ? 8 : 4;  // elements per 16 bytes
   if (split_stride % qa || split_stride < rows * head_dim)
     return fail(SPS_EINVAL, "split_stride must be a multiple of %lld and >= rows*head_dim",
                 (long long)qa);
@@ -541,10 +548,15 @@ sps_status combine_common(int64_t rows, int32_t splits, int32_t head_dim, const 
   if (out_row_stride < head_dim || out_row_stride % 8)
     return fail(SPS_EINVAL, "out_row_stride must be >= head_dim and a multiple of 8");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (bf16p)
+  if (ptype == 1)
     return launched(launch_combine_bf16p(rows, splits, head_dim, partial, split_stride, lse,
                                          lse_split_stride, out_bf16, out_row_stride, out_lse,
                                          dev_status, s),
+                    "combine launch");
+  if (ptype == 2)
+    return launched(launch_combine_f16p(rows, splits, head_dim, partial, split_stride, lse,
+                                        lse_split_stride, out_bf16, out_row_stride, out_lse,
+                                        dev_status, s),
                     "combine launch");
   return launched(launch_combine(rows, splits, head_dim, static_cast<const float*>(partial),
                                  split_stride, lse, lse_split_stride, out_bf16, out_row_stride,
@@ -590,7 +602,7 @@ sps_status partial_combine(int64_t rows, int32_t splits, int32_t head_dim, const
                            void* out_bf16, int64_t out_row_stride, float* out_lse,
                            int32_t* dev_status, sps_stream_t stream) {
   return combine_common(rows, splits, head_dim, partial, split_stride, lse, lse_split_stride,
-                        out_bf16, out_row_stride, out_lse, dev_status, stream, false);
+                        out_bf16, out_row_stride, out_lse, dev_status, stream, 0);
 }
 
 sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
@@ -599,7 +611,26 @@ sps_status partial_combine_bf16(int64_t rows, int32_t splits, int32_t head_dim,
                                 float* out_lse, int32_t* dev_status, sps_stream_t stream) {
   return combine_common(rows, splits, head_dim, partial_bf16, split_stride, lse,
                         lse_split_stride, out_bf16, out_row_stride, out_lse, dev_status, stream,
-                        true);
+                        1);
+}
+
+sps_status sparse_prefill_fwd_f16(const sps_plan* pl, const void* q, float q_scale,
+                                  const void* k_cache, const void* v_cache, const void* k_scales,
+                                  const void* v_scales, const int32_t* page_table,
+                                  const int32_t* idx, void* partial_f16, int64_t split_stride,
+                                  float* lse, int64_t lse_split_stride, void* ws,
+                                  sps_stream_t stream) {
+  return fwd_common(pl, q, q_scale, k_cache, v_cache, k_scales, v_scales, page_table, idx,
+                    partial_f16, split_stride, lse, lse_split_stride, ws, stream,
+                    FwdKind::kF16Partials);
+}
+
+sps_status partial_combine_f16(int64_t rows, int32_t splits, int32_t head_dim,
+                               const void* partial_f16, int64_t split_stride, const float* lse,
+                               int64_t lse_split_stride, void* out_bf16, int64_t out_row_stride,
+                               float* out_lse, int32_t* dev_status, sps_stream_t stream) {
+  return combine_common(rows, splits, head_dim, partial_f16, split_stride, lse, lse_split_stride,
+                        out_bf16, out_row_stride, out_lse, dev_status, stream, 2);
 }
 
 sps_status sps_kv_append(const sps_plan* pl, const void* k_new, const void* v_new,

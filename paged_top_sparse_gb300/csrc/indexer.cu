@@ -225,10 +225,16 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int quarter = warp % 4;          // TMEM lanes 32*quarter ...
     const int row = quarter * 32 + lane;   // tile row = token within the tile
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    // Every item of a plan has the same head count (two when the group's query-head count is
+    // even).  With one head, the second warpgroup has no accumulator to read and nothing waits
+    // for its arrivals, so it takes no part: a warpgroup that only waited and arrived could fall
+    // a whole ring behind the K barriers and then mistake a later phase for the one it wants.
+    const int nh_plan = (p.Hg % 2 == 0) ? 2 : 1;
+    const int n_items = e < nh_plan ? p.n_idx_tasks : 0;
     uint32_t jp = 0;
     // both accumulators start free (page pair 0)
-    if (lane == 0) mbar_arrive(smem_u32(e == 0 ? &sm.k_full[0] : &sm.a1_free[0]));
-    for (int ti = blockIdx.x; ti < p.n_idx_tasks; ti += gridDim.x) {
+    if (lane == 0 && e < nh_plan) mbar_arrive(smem_u32(e == 0 ? &sm.k_full[0] : &sm.a1_free[0]));
+    for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
       const IdxTask t = p.idx_tasks[ti];
       const ReqInfo ri = p.reqs[t.req];
       const bool valid = row < t.ntok && e < t.nh;

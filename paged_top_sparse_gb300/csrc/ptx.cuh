@@ -374,6 +374,35 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ quantised formats
+// Two E4M3 codes (low byte = first element) -> f16x2 (low half = first element); exact.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+// Two E2M1 codes in one byte (low nibble = first element) -> f16x2; exact.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(uint16_t byte_in_low) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tmov.b16 {t, _}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "h"(byte_in_low));
+  return r;
+}
+// f16x2 product (round to nearest; exact for an E2M1 code times an E4M3 scale: at most 6
+// significant bits, magnitudes in [2^-10, 2688]).
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// f16x2 -> two E4M3 codes (nearest even, saturating at +-448), low half -> low byte.
+__device__ __forceinline__ uint16_t cvt_f16x2_e4m3x2(uint32_t h) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(h));
+  return e;
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled tile whose
 // rows are 128 bytes long (the layout TMA writes with SWIZZLE_128B and the tensor core reads
 // with a SWIZZLE_128B descriptor): chunks are XOR-permuted by the row index mod 8.

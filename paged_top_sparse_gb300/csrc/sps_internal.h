@@ -62,11 +62,11 @@ struct DevPlan {
   int32_t* bucket_totals;   // [num_buckets]: entries per bucket (single-launch inversion)
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
-  // FP16 copies of quantised inputs (null when the plan has none): Q [T][H][D] and K, V
-  // caches [num_phys][H_kv][128][D]; each call that needs one converts into it first
+  // FP16 copies of quantised inputs (null when the plan has none): Q [T][H][D], and the K
+  // cache [num_phys][H_kv][128][D] for an NVFP4 indexer; each call that needs one converts
+  // into it first
   void* qconv;
   void* kconv;
-  void* vconv;
 };
 
 // Launchers (one per kernel file).  Return cudaSuccess or the launch error.
@@ -93,6 +93,12 @@ cudaError_t launch_forward_bf16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, 
                                  const void* vs, const int32_t* page_table, void* partial,
                                  int64_t split_stride, float* lse, int64_t lse_split_stride,
                                  cudaStream_t st);
+// The same forward with FP16 partials (split stride in elements).
+cudaError_t launch_forward_f16p(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
+                                float q_scale, const void* kc, const void* vc, const void* ks,
+                                const void* vs, const int32_t* page_table, void* partial,
+                                int64_t split_stride, float* lse, int64_t lse_split_stride,
+                                cudaStream_t st);
 // The pages' Q8KV4 route: K rounded to E4M3, S = Q K^T on the FP8 tensor core (D = 128).
 cudaError_t launch_forward_fp8qk(const DevPlan& p, sps_dtype qt, sps_dtype kvt, const void* q,
                                  float q_scale, const void* kc, const void* vc, const void* ks,
@@ -104,6 +110,12 @@ cudaError_t launch_combine_bf16p(int64_t rows, int32_t splits, int32_t D, const 
                                  int64_t split_stride, const float* lse, int64_t lse_split_stride,
                                  void* out, int64_t out_row_stride, float* out_lse,
                                  int32_t* status, cudaStream_t st);
+
+// The combine over FP16 partials.
+cudaError_t launch_combine_f16p(int64_t rows, int32_t splits, int32_t D, const void* partial,
+                                int64_t split_stride, const float* lse, int64_t lse_split_stride,
+                                void* out, int64_t out_row_stride, float* out_lse,
+                                int32_t* status, cudaStream_t st);
 
 // Chunked-prefill append of the new tokens' K/V into the paged cache (BF16 copy or NVFP4
 // quantisation), per-tensor E4M3 quantisation, and the BF16 absmax behind its scale.

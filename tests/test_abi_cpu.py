@@ -77,5 +77,23 @@ def test_combine_validation_needs_no_device(L):
     assert L.partial_combine(0, 16, 128, None, 0, None, 0, None, 128, None, None, None) == 0
     assert L.partial_combine(10, 0, 128, None, 0, None, 0, None, 128, None, None, None) == 1
     assert L.partial_combine(10, 4, 96, None, 0, None, 0, None, 128, None, None, None) == 2
-    fake = ctypes.c_void_p(1 << 20)
-    assert L.partial_combine(10, 4, 128, fake, 100, fake, 10, fake, 128, None, None, None) == 1
+    # a split stride below rows * head_dim: real buffers large enough for every element the
+    # declared strides reach, so the call stays in bounds whatever the order of the checks
+    rows, splits, d, stride = 10, 4, 128, 100
+    part = np.zeros((splits - 1) * stride + rows * d, dtype=np.float32)
+    lse = np.zeros(splits * rows, dtype=np.float32)
+    out = np.zeros(rows * d, dtype=np.uint16)
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    assert L.partial_combine(rows, splits, d, ptr(part), stride, ptr(lse), rows, ptr(out), d,
+                             None, None, None) == 1
+    assert b"split_stride" in L.sps_last_error()
+
+
+def test_plan_rejects_more_than_512_pages_per_request(L):
+    """The top-k lane layouts and the inversion windows are sized for at most 512 visible pages
+    (64K tokens of context per request); a plan beyond that is refused with a message."""
+    _plan(q_lens=[200], ctx_lens=[65300], max_pages_per_req=512, num_phys_pages=512)
+    with pytest.raises(B.SpsError) as e:
+        _plan(q_lens=[200], ctx_lens=[65400], max_pages_per_req=513, num_phys_pages=513)
+    assert e.value.status == 2
+    assert "512" in str(e.value)
