@@ -7,8 +7,10 @@
 //                  block (cvt to FP16), one FP16 multiply that is exact: the product has at
 //                  most 6 significant bits and lies within [2^-10, 2688].
 //
-// Streaming kernels (grid-stride, 16 elements per thread per step); the indexer and the
-// forward run them on quantised inputs before their FP16 tensor-core paths.
+// Streaming kernels (grid-stride, 16 elements per thread per step): the E4M3 query copy that
+// the FP16 tensor-core paths read, the public sps_dequantize, and, for an indexer over NVFP4
+// keys, the batch's visible key pages gathered through the page table into logical order (the
+// forward dequantises its K/V tiles inside its own loader instead).
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -81,7 +83,52 @@ nvfp4_to_e4m3_kernel(const uint2* __restrict__ codes, const uint8_t* __restrict_
   }
 }
 
+// The batch's visible key pages, in logical order: block (global page slot gp, KV head g)
+// converts the NVFP4 tile of physical page page_table[req][pg] into tile gp * H_kv + g of `out`
+// (FP16 [total_pages][H_kv][128][D]).  A page-table entry outside [0, num_phys_pages) raises
+// DEV_BAD_PAGE and converts page 0 instead.
+__global__ void __launch_bounds__(256)
+nvfp4_pages_to_f16_kernel(DevPlan p, const uint2* __restrict__ codes,
+                          const uint8_t* __restrict__ scales, const int32_t* __restrict__ pt,
+                          uint4* __restrict__ out) {
+  const int gp = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+  const int req = p.page_req[gp];
+  const int pg = gp - p.reqs[req].page_base;
+  int phys = __ldg(pt + (int64_t)req * p.max_pages + pg);
+  if (phys < 0 || phys >= p.num_phys) {
+    if (threadIdx.x == 0) set_status(p.status, DEV_BAD_PAGE);
+    phys = 0;
+  }
+  const int nb = 128 * p.D / 16;  // 16-element blocks of one tile
+  const int64_t src = (int64_t)(phys * p.Hkv + g) * nb;
+  const int64_t dst = (int64_t)blockIdx.x * nb;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    const uint2 c = __ldg(codes + src + i);
+    const uint8_t sb = __ldg(scales + src + i);
+    const uint32_t s2 = cvt_e4m3x2((uint16_t)(sb | (sb << 8)));
+    const uint32_t w[2] = {c.x, c.y};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        h[4 * j + b] = hmul2_u32(cvt_e2m1x2((uint16_t)((w[j] >> (8 * b)) & 0xff)), s2);
+    out[2 * (dst + i)] = make_uint4(h[0], h[1], h[2], h[3]);
+    out[2 * (dst + i) + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_pages(const DevPlan& p, const void* codes, const void* scales,
+                                 const int32_t* page_table, void* out, cudaStream_t st) {
+  const int64_t tiles = (int64_t)p.total_pages * p.Hkv;
+  if (tiles <= 0) return cudaSuccess;
+  nvfp4_pages_to_f16_kernel<<<(unsigned)tiles, 256, 0, st>>>(
+      p, static_cast<const uint2*>(codes), static_cast<const uint8_t*>(scales), page_table,
+      static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dequant_e4m3(const void* in, const void* scales, int64_t n, void* out,
                                 cudaStream_t st) {

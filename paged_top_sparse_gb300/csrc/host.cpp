@@ -307,14 +307,16 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
   // FP16 staging of quantised inputs for the tensor-core paths: an exact FP16 copy of E4M3 Q;
-  // the indexer with NVFP4 keys also takes an FP16 copy of the key cache.  The forward
-  // dequantises NVFP4 K/V inside its loader and needs no copy of the caches.  (E4M3 x E4M3
-  // indexing runs on the FP8 tensor core directly and needs none.)
+  // an indexer over NVFP4 keys also takes FP16 copies of the key tiles of the pages the batch
+  // sees (every one of them is read by the indexer), so the workspace grows with the batch,
+  // not with the physical pool.  The forward dequantises NVFP4 K/V inside its loader, and
+  // E4M3 x E4M3 indexing runs on the FP8 tensor core directly; neither needs a copy.
   const bool idx_fp16 = p.idx_k_dtype == SPS_NVFP4;
-  const int64_t cache_elems = (int64_t)p.num_phys_pages * p.num_kv_heads * kPage * p.head_dim;
   if (p.q_dtype == SPS_E4M3 || (idx_fp16 && p.idx_q_dtype == SPS_E4M3))
     pl->off_qconv = take(2 * pl->R * p.head_dim);
-  if (idx_fp16) pl->off_kconv = take(2 * cache_elems);
+  if (idx_fp16)
+    pl->off_kconv = take(2 * std::max<int64_t>(1, pl->total_pages) * p.num_kv_heads * kPage *
+                         p.head_dim);
   pl->ws_bytes = off;
 
   // the host image of [0, upload_end): the status word and counters (zero), then the metadata

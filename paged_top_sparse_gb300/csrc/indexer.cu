@@ -59,7 +59,7 @@ template <int ROWB, bool FP8, bool BF16IN>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                DevPlan p, const int32_t* __restrict__ page_table, float* __restrict__ scores,
-               int64_t pitch, float qk_scale) {
+               int64_t pitch, float qk_scale, int logical_keys) {
   using Smem = IdxSmem<ROWB>;
   constexpr int DB = ROWB / 128;       // 128-byte column blocks per row
   constexpr int KSTEPS = DB * 4;       // 32-byte K steps per row
@@ -135,8 +135,9 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           const uint32_t kf = smem_u32(&sm.k_full[ks]);
           mbar_expect_tx(kf, npg * TILE);
           for (int u = 0; u < npg; ++u) {
-            int phys = __ldg(pt_row + pb + u);
-            if (phys < 0 || phys >= p.num_phys) {
+            // logical_keys: the key tiles were copied in logical page order (global page slot)
+            int phys = logical_keys ? p.reqs[t.req].page_base + pb + u : __ldg(pt_row + pb + u);
+            if (!logical_keys && (phys < 0 || phys >= p.num_phys)) {
               set_status(status, DEV_BAD_PAGE);
               phys = 0;
             }
@@ -303,7 +304,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 template <int ROWB, bool FP8, bool BF16IN>
 cudaError_t run_indexer(const DevPlan& p, int tm_dtype, const void* q, const void* kc,
                         const int32_t* page_table, float* scores, int64_t pitch, float scale,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool logical_keys = false) {
   const int EB = FP8 ? 1 : 2;
   alignas(64) CUtensorMap tmQ, tmK;
   const uint32_t box_inner = 128 / EB;
@@ -311,15 +312,17 @@ cudaError_t run_indexer(const DevPlan& p, int tm_dtype, const void* q, const voi
                       (uint64_t)p.T, (uint64_t)p.D * EB, (uint64_t)p.H * p.D * EB, box_inner, 1,
                       128, true))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tmK, tm_dtype, const_cast<void*>(kc), (uint64_t)p.D,
-                      (uint64_t)p.num_phys * p.Hkv * 128, (uint64_t)p.D * EB, box_inner, 128, true))
+  const uint64_t key_tiles = (uint64_t)(logical_keys ? p.total_pages : p.num_phys) * p.Hkv;
+  if (!encode_tmap_2d(&tmK, tm_dtype, const_cast<void*>(kc), (uint64_t)p.D, key_tiles * 128,
+                      (uint64_t)p.D * EB, box_inner, 128, true))
     return cudaErrorInvalidValue;
   const int smem = (int)sizeof(IdxSmem<ROWB>) + 1024;
   auto kern = indexer_kernel<ROWB, FP8, BF16IN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(p.n_idx_tasks, num_sms()));
-  kern<<<grid, kThreads, smem, st>>>(tmQ, tmK, p, page_table, scores, pitch, scale);
+  kern<<<grid, kThreads, smem, st>>>(tmQ, tmK, p, page_table, scores, pitch, scale,
+                                     logical_keys ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -337,17 +340,20 @@ cudaError_t launch_indexer(const DevPlan& p, sps_dtype qt, sps_dtype kt, const v
   if (qt == SPS_E4M3 && kt == SPS_E4M3 && p.D == 128)
     return run_indexer<128, true, false>(p, 2, q, kc, page_table, scores, pitch, scale, st);
   if (qt == SPS_E4M3 && kt == SPS_NVFP4) {
-    // E4M3 codes and NVFP4 products are exact in FP16: convert both, then the FP16 MMA path
-    // (the per-tensor scales stay in the FP32 epilogue)
+    // E4M3 codes and NVFP4 products are exact in FP16: convert Q, and the key tiles of the
+    // pages the batch sees (through the page table, into logical order: every one of them is
+    // read, by many query tiles, so each is converted once rather than in every loader), then
+    // the FP16 MMA path (the per-tensor scales stay in the FP32 epilogue)
     if (!p.qconv || !p.kconv) return cudaErrorInvalidValue;
     cudaError_t e = launch_dequant(SPS_E4M3, q, nullptr, (int64_t)p.T * p.H * p.D, p.qconv, st);
     if (e != cudaSuccess) return e;
-    e = launch_dequant(SPS_NVFP4, kc, kscales, (int64_t)p.num_phys * p.Hkv * 128 * p.D, p.kconv,
-                       st);
+    e = launch_dequant_pages(p, kc, kscales, page_table, p.kconv, st);
     if (e != cudaSuccess) return e;
     if (p.D == 128)
-      return run_indexer<256, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch, scale, st);
-    return run_indexer<128, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch, scale, st);
+      return run_indexer<256, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch,
+                                            scale, st, true);
+    return run_indexer<128, false, false>(p, 1, p.qconv, p.kconv, page_table, scores, pitch,
+                                          scale, st, true);
   }
   return cudaErrorNotSupported;
 }

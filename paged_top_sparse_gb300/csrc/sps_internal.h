@@ -62,9 +62,10 @@ struct DevPlan {
   int32_t* bucket_totals;   // [num_buckets]: entries per bucket (single-launch inversion)
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
-  // FP16 copies of quantised inputs (null when the plan has none): Q [T][H][D], and the K
-  // cache [num_phys][H_kv][128][D] for an NVFP4 indexer; each call that needs one converts
-  // into it first
+  // FP16 copies of quantised inputs (null when the plan has none), each rewritten by the call
+  // that reads it: Q [T][H][D]; for an indexer over NVFP4 keys, the key tiles of the batch's
+  // visible pages in logical order [total_pages][H_kv][128][D] (global page slot = request's
+  // page_base + logical page)
   void* qconv;
   void* kconv;
 };
@@ -138,6 +139,10 @@ cudaError_t launch_barrier_timeout(unsigned int* bar, int32_t* status, int64_t l
 // Exact E4M3 / NVFP4 -> FP16 conversion of n elements (n % 16 == 0).
 cudaError_t launch_dequant(sps_dtype dt, const void* in, const void* scales, int64_t n,
                            void* out, cudaStream_t st);
+// NVFP4 key tiles of the batch's visible pages, through the page table, into the plan's
+// logical-order FP16 copy (DevPlan::kconv).
+cudaError_t launch_dequant_pages(const DevPlan& p, const void* codes, const void* scales,
+                                 const int32_t* page_table, void* out, cudaStream_t st);
 // NVFP4 -> E4M3 codes: each exact code x scale product rounded to nearest even E4M3
 // (saturating), the pages' QMUL4 dequant.
 cudaError_t launch_dequant_e4m3(const void* in, const void* scales, int64_t n, void* out,
