@@ -10,6 +10,12 @@ buffers (H2D of Q/K/V/page table and D2H of the output inside the timed region),
 step's copies on their own streams overlapping the neighbouring steps' compute; the serial
 form (copy in, step, copy out, one after another) is reported beside it.
 
+The default line (the 8K BF16 prefill with FP32 partials) also carries, under ``configs``, the
+same measurement of every other configuration of the method's workloads: the 8K prefill with
+FP16 and with BF16 partials, the quantised 8K prefill (exact route and the FP8 route), the
+combine stress (a 4.3 GB FP32 partial buffer) and the chunked batch (8 x 512 new tokens over
+~32K of context); ``--no-configs`` skips them.
+
 ``--impl reference`` times the FP64 CPU oracle instead (a bounded row sample per step).
 
 Prints one JSON line (rank 0).
@@ -154,16 +160,6 @@ def _algorithmic(w, idx_np, partial_bytes=4):
 
 
 WORKLOADS = ("prefill8k", "prefill8k_q", "chunked32k", "combine_stress", "kv_append")
-
-
-def _workload(args):
-    from paged_top_sparse_gb300 import synth
-
-    if args.workload == "prefill8k" and args.tokens != 8192:
-        # same shape with another prefill length (used for profiling captures)
-        return synth.workload("custom", seed=args.seed, q_lens=[args.tokens], ctx_lens=[0],
-                              num_q_heads=32, num_kv_heads=2, head_dim=128, top_k=16)
-    return synth.workload(args.workload, seed=args.seed)
 
 
 def _describe(w, name):
@@ -324,23 +320,37 @@ def _e2e_pipelined(args, flush, stream, in_pairs, step, copy_out, nbuf=2):
     return t0.elapsed_time(t1) / args.steps
 
 
-def run_gpu(args, rank, world):
+def _launches_per_step(w, fp8qk, inv_launches):
+    """Kernels of this library one step launches: plan upload, indexer, top-k, the inversion
+    (one cooperative launch, or three kernels), forward, combine, plus the quantised paths'
+    copies (the indexer's FP16 Q and visible key pages over NVFP4 keys; the forward's FP16 Q
+    on the exact route)."""
+    n = 5 + inv_launches
+    if w.idx_dtype != "e4m3" and w.kv_dtype == "nvfp4":
+        n += 2
+    if w.q_dtype == "e4m3" and not fp8qk:
+        n += 1
+    return n
+
+
+def run_prefill(args, world, dev, wname, partials="fp32", fp8qk=False, data=None):
+    """One workload through the four C-ABI calls: the device-timed step, the end-to-end step
+    from pinned host buffers, and the per-kernel roofline fractions.  Returns (line, w, t)."""
     import torch
 
     from paged_top_sparse_gb300 import binding as B
-    from paged_top_sparse_gb300 import build
-
-    build.build()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    if args.workload == "combine_stress":
-        return run_combine_stress(args, rank, world, dev)
-    if args.workload == "kv_append":
-        return run_kv_append(args, rank, world, dev)
     from paged_top_sparse_gb300 import synth
 
-    w = _workload(args)
-    t = synth.make_tensors(w)
+    if data is None:
+        if wname == "prefill8k" and args.tokens != 8192:
+            # same shape with another prefill length (used for profiling captures)
+            w = synth.workload("custom", seed=args.seed, q_lens=[args.tokens], ctx_lens=[0],
+                               num_q_heads=32, num_kv_heads=2, head_dim=128, top_k=16)
+        else:
+            w = synth.workload(wname, seed=args.seed)
+        t = synth.make_tensors(w)
+    else:
+        w, t = data
     R, K, D = w.num_rows, w.top_k, w.head_dim
     host = _host_inputs(w, t)
     hin = {k: _pinned(v) for k, v in host.items()}
@@ -356,21 +366,21 @@ def run_gpu(args, rank, world):
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     scores = torch.empty((R, w.max_pages), dtype=torch.float32, device=dev)
     idx = torch.empty((R, K), dtype=torch.int32, device=dev)
-    bf16p = args.partials != "fp32"  # 16-bit partial storage (BF16 or FP16)
-    pdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.partials]
+    p16 = partials != "fp32"  # 16-bit partial storage (BF16 or FP16)
+    pdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[partials]
     partial = torch.empty((K, R, D), dtype=pdt, device=dev)
     lse = torch.empty((K, R), dtype=torch.float32, device=dev)
     out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     fwd_call = {"fp32": B.sparse_prefill_fwd, "bf16": B.sparse_prefill_fwd_bf16,
-                "f16": B.sparse_prefill_fwd_f16}[args.partials]
-    if args.fp8qk:
-        if bf16p or w.kv_dtype != "nvfp4":
+                "f16": B.sparse_prefill_fwd_f16}[partials]
+    if fp8qk:
+        if p16 or w.kv_dtype != "nvfp4":
             raise SystemExit("--fp8qk needs the quantised workload (prefill8k_q) and FP32 partials")
         fwd_call = B.sparse_prefill_fwd_fp8qk
     combine_call = {"fp32": B.partial_combine, "bf16": B.partial_combine_bf16,
-                    "f16": B.partial_combine_f16}[args.partials]
+                    "f16": B.partial_combine_f16}[partials]
 
     def step(ev, di=din, out_=out):
         pl = B.Plan(*plan_args, **plan_kw)
@@ -420,8 +430,9 @@ def run_gpu(args, rank, world):
 
     step_ms, e2e_ms, e2e_serial_ms = max_over_ranks([step_ms, e2e_ms, e2e_serial_ms], world)
 
-    alg = _algorithmic(w, idx.cpu().numpy(), partial_bytes=2 if bf16p else 4)
+    alg = _algorithmic(w, idx.cpu().numpy(), partial_bytes=2 if p16 else 4)
     hbm, bf16, peak_kind = _peaks()
+    src = "measured (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
     idx_peak = bf16 * 2 if idx_fp8 else bf16  # FP8 tensor rate: the nominal 2x of BF16
     k_ms = per.mean(0)
     names = ["indexer", "topk", "fwd", "combine"]
@@ -432,14 +443,16 @@ def run_gpu(args, rank, world):
     inv_launches = 1 if inv_blocks <= 8 * torch.cuda.get_device_properties(dev).multi_processor_count else 3
     kern = {
         "indexer": {"us": k_ms[0] * 1e3, "achieved": alg["indexer_flops"] / (k_ms[0] * 1e-3) / 1e12,
-                    "unit": "TFLOP/s", "peak": idx_peak, "bound": "tensor"},
+                    "unit": "TFLOP/s", "peak": idx_peak, "bound": "tensor",
+                    "peak_source": ("2 x " + src + " BF16 (nominal FP8/BF16 rate ratio)")
+                    if idx_fp8 else src + " BF16"},
         "topk": {"us": k_ms[1] * 1e3, "achieved": alg["topk_bytes"] / (k_ms[1] * 1e-3) / 1e9,
-                 "unit": "GB/s", "peak": hbm, "bound": "hbm"},
+                 "unit": "GB/s", "peak": hbm, "bound": "hbm", "peak_source": src + " HBM"},
         "fwd": {"us": k_ms[2] * 1e3, "achieved": alg["fwd_bytes"] / (k_ms[2] * 1e-3) / 1e9,
-                "unit": "GB/s", "peak": hbm, "bound": "hbm",
+                "unit": "GB/s", "peak": hbm, "bound": "hbm", "peak_source": src + " HBM",
                 "tensor_tflops": alg["fwd_flops"] / (k_ms[2] * 1e-3) / 1e12},
         "combine": {"us": k_ms[3] * 1e3, "achieved": alg["combine_bytes"] / (k_ms[3] * 1e-3) / 1e9,
-                    "unit": "GB/s", "peak": hbm, "bound": "hbm"},
+                    "unit": "GB/s", "peak": hbm, "bound": "hbm", "peak_source": src + " HBM"},
     }
     for v in kern.values():
         v["frac"] = v["achieved"] / v["peak"]
@@ -448,12 +461,13 @@ def run_gpu(args, rank, world):
     kern["fwd"]["tensor_frac"] = round(kern["fwd"]["tensor_tflops"] / bf16, 4)
     dom = names[int(np.argmax(k_ms))]
     traffic = None
-    if args.workload == "prefill8k" and args.tokens == 8192 and not bf16p:  # counters' workload
+    if wname == "prefill8k" and args.tokens == 8192 and not p16:  # the counters' workload
         try:
             with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
                 traffic = json.load(f).get(dom)
         except Exception:
             pass
+    storage = {"bf16": ", BF16 partials", "f16": ", FP16 partials"}.get(partials, "")
     line = {
         "metric": METRIC,
         "value": round(job_tokens_per_s(w.num_tokens, world, step_ms), 1),
@@ -468,18 +482,16 @@ def run_gpu(args, rank, world):
         "dtype": "fp16" if w.kv_dtype == "nvfp4" else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, quantised where the workload says; permuted "
                 "page table)",
-        "config": {"workload": _describe(w, args.workload)
-                               + ({"bf16": ", BF16 partials", "f16": ", FP16 partials"}.get(args.partials, ""))
-                               + (", FP8 Q K^T on E4M3-rounded K" if args.fp8qk else ""),
-                   "partials": args.partials,
+        "config": {"workload": _describe(w, wname) + storage
+                               + (", FP8 Q K^T on E4M3-rounded K" if fp8qk else ""),
+                   "partials": partials,
                    "batch": int(w.batch), "seq_len": int(max(w.q_lens)), "rows": int(R),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (256 MB write); per-step CUDA events"},
         "roofline": {"bound": kern[dom]["bound"], "kernel": dom,
                      "achieved": kern[dom]["achieved"], "peak": kern[dom]["peak"],
                      "unit": kern[dom]["unit"], "frac": kern[dom]["frac"],
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback",
-                     "traffic": traffic},
+                     "peak_source": kern[dom]["peak_source"], "traffic": traffic},
         "kernels": kern,
         "combine_hbm_gbs": kern["combine"]["achieved"],
         "fwd_tensor_pipe_frac": kern["fwd"]["tensor_frac"],
@@ -491,17 +503,66 @@ def run_gpu(args, rank, world):
                         "copies inside the timed region",
                 "serial_ms_per_step": round(e2e_serial_ms, 4),
                 "serial_value": round(job_tokens_per_s(w.num_tokens, world, e2e_serial_ms), 1)},
-        # plan-upload copy, indexer, top-k, the inversion, forward, combine; plus the dequant
-        # kernels of the quantised path (2 before the indexer; 3 before the forward, or 2 on
-        # the FP8 route)
-        "gpu_launches": (5 + inv_launches
-                         + ((4 if args.fp8qk else 5) if w.kv_dtype == "nvfp4" else 0))
-                        * args.steps,
+        "gpu_launches": _launches_per_step(w, fp8qk, inv_launches) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
         "host": clocks.host,
     }
     return line, w, t
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from paged_top_sparse_gb300 import build
+
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if args.workload == "combine_stress":
+        return run_combine_stress(args, rank, world, dev)
+    if args.workload == "kv_append":
+        return run_kv_append(args, rank, world, dev)
+    return run_prefill(args, world, dev, args.workload, args.partials, args.fp8qk)
+
+
+def _sub(line):
+    """The fields of a workload's line that the headline's `configs` key carries."""
+    keys = ("value", "unit", "ms_per_step", "dtype", "roofline", "kernels", "e2e",
+            "gpu_launches", "clocks")
+    d = {k: line[k] for k in keys if k in line}
+    d["workload"] = line["config"]["workload"]
+    d["tokens_per_s"] = d.pop("value")
+    return d
+
+
+def run_other_configs(args, world, w0, t0):
+    """Every other configuration of the method's workloads, each timed like the headline:
+    the 8K prefill with 16-bit partials (FP16, BF16), the quantised 8K prefill (exact route
+    and the FP8 route), the combine stress and the chunked 8 x 512-over-32K batch."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    out = {}
+    for key, wname, partials, fp8 in (("prefill8k_f16_partials", "prefill8k", "f16", False),
+                                      ("prefill8k_bf16_partials", "prefill8k", "bf16", False)):
+        line, _, _ = run_prefill(args, world, dev, wname, partials, fp8, data=(w0, t0))
+        out[key] = _sub(line)
+        torch.cuda.empty_cache()
+    data = None
+    for key, fp8 in (("prefill8k_q", False), ("prefill8k_q_fp8qk", True)):
+        line, w, t = run_prefill(args, world, dev, "prefill8k_q", "fp32", fp8, data=data)
+        data = (w, t)
+        out[key] = _sub(line)
+        torch.cuda.empty_cache()
+    del data
+    line, _, _ = run_combine_stress(args, 0, world, dev)
+    out["combine_stress"] = _sub(line)
+    torch.cuda.empty_cache()
+    line, _, _ = run_prefill(args, world, dev, "chunked32k")
+    out["chunked32k"] = _sub(line)
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_combine_stress(args, rank, world, dev):
@@ -560,9 +621,12 @@ def run_combine_stress(args, rank, world, dev):
                    "l2": "inputs (4.3 GB) far larger than L2; 256 MB flush between steps"},
         "roofline": {"bound": "hbm", "kernel": "combine", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)"
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst) HBM"
                      if peak_kind == "measured" else "fallback",
                      "traffic": None},
+        "kernels": {"combine": {"us": round(comb_ms * 1e3, 4), "achieved": round(achieved, 1),
+                                "unit": "GB/s", "peak": hbm, "bound": "hbm",
+                                "frac": round(achieved / hbm, 4)}},
         "combine_hbm_gbs": round(achieved, 1),
         "e2e": {"value": round(job_tokens_per_s(T, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
@@ -716,6 +780,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="headline workload only: skip the other configurations that the "
+                         "default line carries under `configs`")
     ap.add_argument("--h2d-streams", type=int, default=1,
                     help="streams that share each step's host-to-device input copies in the "
                          "pipelined end-to-end measurement")
@@ -749,6 +816,10 @@ def main():
             print(json.dumps(run_reference(args, rank, 1), default=_json_default))
         return
     line, w, t = run_gpu(args, rank, world)
+    default_line = (args.workload == "prefill8k" and args.tokens == 8192
+                    and args.partials == "fp32" and not args.fp8qk)
+    if default_line and not args.no_configs:
+        line["configs"] = run_other_configs(args, world, w, t)
     if rank == 0:
         if not args.no_cpu_baseline and w is not None:
             line["cpu_baseline"] = cpu_baseline(w, t, budget_s=float(os.environ.get("SPS_CPU_S", "12")))
