@@ -75,6 +75,7 @@ combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();  // the prologue may overlap the previous kernel (the forward)
 
   if (warp == 8) {
     // ---------------- producer warp
@@ -246,18 +247,12 @@ cudaError_t launch_combine_t(int64_t rows, int32_t splits, int32_t D, const P* p
   int64_t grid = std::min<int64_t>(ntiles, 3LL * num_sms());
   if (grid < 1) return cudaSuccess;
   auto* o = static_cast<__nv_bfloat16*>(out);
-  if (D == 128) {
-    cudaFuncSetAttribute(combine_kernel<128, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    combine_kernel<128, P><<<(unsigned)grid, kThreads, smem, st>>>(
-        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
-        status);
-  } else {
-    cudaFuncSetAttribute(combine_kernel<64, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    combine_kernel<64, P><<<(unsigned)grid, kThreads, smem, st>>>(
-        rows, splits, partial, split_stride, lse, lse_split_stride, o, out_row_stride, out_lse,
-        status);
-  }
-  return cudaGetLastError();
+  auto kern = D == 128 ? combine_kernel<128, P> : combine_kernel<64, P>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, rows, splits, partial,
+                 split_stride, lse, lse_split_stride, o, out_row_stride, out_lse, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

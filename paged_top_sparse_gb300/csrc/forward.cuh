@@ -180,7 +180,6 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                                       ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   int32_t* status = p.status;
-  const int ntasks = *(volatile int32_t*)(p.counters + 2);
   const int64_t R = (int64_t)p.T * p.H;
 
   if (tid == 0) {
@@ -217,6 +216,11 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above may overlap the previous kernel (the inversion); from here on the
+  // kernel reads what it wrote
+  pdl_wait();
+  pdl_trigger();
+  const int ntasks = *(volatile int32_t*)(p.counters + 2);
   const uint32_t tmem = sm.tmem_base;  // S[b] at column 128 b, O[b] at 256 + 128 b
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -676,11 +680,11 @@ cudaError_t run_forward(const DevPlan& p, const void* q, const void* kc, const v
   auto kern = forward_kernel<D, MODE, PT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, smem, st>>>(
-      tmQ, tmK, tmV, p, static_cast<const uint8_t*>(kc), static_cast<const uint8_t*>(ks),
-      static_cast<const uint8_t*>(vc), static_cast<const uint8_t*>(vs), page_table, partial,
-      split_stride, lse, lse_split_stride, q_scale);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(num_sms()), dim3(kThreads), smem, st, tmQ, tmK, tmV, p,
+                 static_cast<const uint8_t*>(kc), static_cast<const uint8_t*>(ks),
+                 static_cast<const uint8_t*>(vc), static_cast<const uint8_t*>(vs), page_table,
+                 partial, split_stride, lse, lse_split_stride, q_scale);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The forward for a plan's dtypes: BF16 Q/K/V, or E4M3 Q (an exact FP16 copy in the

@@ -96,6 +96,10 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the prologue above may overlap the previous kernel (the plan upload); from here on the
+  // kernel reads what it wrote
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = sm.tmem_base;  // head h's accumulator: columns 256 h .. 256 h + 255
   volatile int* abort_flag = &sm.abort_flag;
 
@@ -321,9 +325,9 @@ cudaError_t run_indexer(const DevPlan& p, int tm_dtype, const void* q, const voi
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(p.n_idx_tasks, num_sms()));
-  kern<<<grid, kThreads, smem, st>>>(tmQ, tmK, p, page_table, scores, pitch, scale,
-                                     logical_keys ? 1 : 0);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, tmQ, tmK, p, page_table, scores,
+                 pitch, scale, logical_keys ? 1 : 0);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

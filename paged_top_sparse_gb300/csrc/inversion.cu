@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(256, 8)
 emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
   __shared__ int pos0[kInvPages][kChunkWords + 1];  // first entry of (page, warp)
+  pdl_trigger();  // the forward that follows may start its prologue
   int g, c;
   const int b = find_block(p, blockIdx.x, &g, &c);
   if (b < 0) return;  // uniform over the block
@@ -340,6 +341,7 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
   __shared__ int sh[32];
   __shared__ int flag;
   unsigned int* bar = reinterpret_cast<unsigned int*>(p.counters + 4);
+  pdl_trigger();  // the forward that follows may start its prologue
   int g = 0, c = 0;
   const int b = find_block(p, blockIdx.x, &g, &c);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

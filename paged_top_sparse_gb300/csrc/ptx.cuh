@@ -119,6 +119,17 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* bar, int32_t* status,
   return *flag != 0;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch.  pdl_wait: block until the grids this one depends on in the
+// stream have completed and their writes are visible (returns at once when the launch carried
+// no such dependency); every kernel launched with one calls it, on every path, before it reads
+// anything an earlier kernel wrote.  pdl_trigger: let the next grid in the stream begin
+// launching (its prologue) while this one finishes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA / bulk copies
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");

@@ -70,6 +70,25 @@ struct DevPlan {
   void* kconv;
 };
 
+// Launch of `kern` that may overlap the previous kernel in the stream (programmatic stream
+// serialization): its blocks can start, and run their prologue, as the previous kernel's
+// blocks leave the SMs; the kernel calls pdl_wait() before it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Launchers (one per kernel file).  Return cudaSuccess or the launch error.
 cudaError_t launch_combine(int64_t rows, int32_t splits, int32_t D, const float* partial,
                            int64_t split_stride, const float* lse, int64_t lse_split_stride,

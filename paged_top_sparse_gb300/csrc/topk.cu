@@ -103,6 +103,7 @@ __device__ __forceinline__ int rounds_lowest_lane(const uint32_t (&key)[E], int 
 template <int E, int KC = 0>  // pages per lane: max_pages <= 32 * E
 __global__ void __launch_bounds__(256)
 topk_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch, int32_t* __restrict__ idx) {
+  pdl_wait();  // the scores come from the indexer just before
   const int lane = threadIdx.x & 31;
   const uint32_t r = blockIdx.x * 8u + (threadIdx.x >> 5);
   if (r >= (uint32_t)p.T * (uint32_t)p.H) return;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(256)
 topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
                    int32_t* __restrict__ idx) {
   __shared__ uint2 cand[8][64];  // per warp: (key, page) of the compacted candidates
+  pdl_wait();  // the scores come from the indexer just before
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t r = blockIdx.x * 8u + warp;  // rows x top_k < 2^31
   if (r >= (uint32_t)p.T * (uint32_t)p.H) return;
@@ -271,25 +273,26 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
   // top_k = 16 (the common case) runs instances whose rounds unroll completely (the filtered
   // long rows do better with the rolled loop)
   const bool k16 = p.K == 16;
+  cudaError_t e;
   if (p.max_pages <= 32) {
-    if (k16) topk_kernel<1, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-    else topk_kernel<1><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    if (k16) e = launch_pdl(topk_kernel<1, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    else e = launch_pdl(topk_kernel<1>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 64) {
-    if (k16) topk_kernel<2, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-    else topk_kernel<2><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    if (k16) e = launch_pdl(topk_kernel<2, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    else e = launch_pdl(topk_kernel<2>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 128) {
-    if (k16) topk_kernel<4, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
-    else topk_kernel<4><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    if (k16) e = launch_pdl(topk_kernel<4, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    else e = launch_pdl(topk_kernel<4>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 256) {
-    topk_filter_kernel<8, 8><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    e = launch_pdl(topk_filter_kernel<8, 8>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 320) {
-    topk_filter_kernel<10, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    e = launch_pdl(topk_filter_kernel<10, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 384) {
-    topk_filter_kernel<12, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    e = launch_pdl(topk_filter_kernel<12, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else {
-    topk_filter_kernel<16, 16><<<grid, 256, 0, st>>>(p, scores, pitch, idx);
+    e = launch_pdl(topk_filter_kernel<16, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace sps

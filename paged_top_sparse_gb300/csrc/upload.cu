@@ -2,6 +2,7 @@
 // directly.  A host-to-device DMA on the copy engine queues behind whatever copies the caller
 // has in flight on other streams (a prefill overlapping the next batch's inputs waits for that
 // whole transfer); loads issued by the SMs do not.
+#include "ptx.cuh"
 #include "sps_internal.h"
 
 namespace sps {
@@ -11,6 +12,7 @@ __global__ void __launch_bounds__(256)
 staged_copy_kernel(const int4* __restrict__ src, int4* __restrict__ dst, int64_t n16,
                    const uint8_t* __restrict__ src_tail, uint8_t* __restrict__ dst_tail,
                    int tail) {
+  pdl_trigger();  // the indexer that follows may start its prologue
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
     dst[i] = src[i];
