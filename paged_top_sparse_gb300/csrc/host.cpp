@@ -132,6 +132,7 @@ struct sps_plan {
   // workspace layout (bytes)
   int64_t off_status = 0, off_counters = 0, off_tok_pos = 0, off_tok_req = 0, off_reqs = 0,
           off_page_req = 0, off_idx_tasks = 0, off_chunk_offsets = 0, off_bucket_totals = 0,
+          off_range_sums = 0,
           off_qconv = -1, off_kconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
   int64_t upload_bytes = 0;  // [0, upload_bytes) of the workspace comes from `blob`
@@ -303,6 +304,7 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   int64_t upload_end = off;
   pl->off_chunk_offsets = take(4 * (pl->num_chunks + 1));
   pl->off_bucket_totals = take(4 * pl->num_buckets);
+  pl->off_range_sums = take(8 * std::max<int64_t>(1, pl->inv_blocks));
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
@@ -391,6 +393,7 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.chunk_offsets = reinterpret_cast<int32_t*>(base + pl->off_chunk_offsets);
   d.bucket_offsets = reinterpret_cast<int32_t*>(base + pl->off_bucket_offsets);
   d.bucket_totals = reinterpret_cast<int32_t*>(base + pl->off_bucket_totals);
+  d.range_sums = reinterpret_cast<int32_t*>(base + pl->off_range_sums);
   d.entries = reinterpret_cast<int2*>(base + pl->off_entries);
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
   d.qconv = pl->off_qconv >= 0 ? base + pl->off_qconv : nullptr;

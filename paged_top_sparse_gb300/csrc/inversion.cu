@@ -396,13 +396,16 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
     if (threadIdx.x == 0) p.bucket_totals[bk] = total;
   }
   if (!grid_barrier(bar, p.status, &flag)) return;
-  // ---- 3. every block: exclusive scans over the bucket totals (entries and work items).
-  // Each thread walks its run of buckets once: it keeps the CSR offsets of this block's own
-  // buckets (its request and KV head, every page) for the emit, and writes the offset and
-  // work items of every gridDim-th bucket.
+  // ---- 3. exclusive scans over the bucket totals (entries and work items), which give every
+  // bucket's CSR offset and its work items.  Few buckets: every block scans them all and keeps
+  // the offsets of its own buckets (its request and KV head, every page) for the emit.  Many
+  // buckets (more than two per thread): each block sums its own range of buckets, a third grid
+  // barrier, then each block scans the ranges' sums (one per block), writes its range's
+  // offsets and work items, and after a fourth barrier reads its own buckets' offsets.
   __shared__ int s_boff[512];  // CSR offset of page pg's bucket of this block's KV head
-  {
-    const int nb = p.num_buckets;
+  const int nb = p.num_buckets;
+  const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
+  if (nb <= 2 * (int)blockDim.x) {
     const int per = (nb + 255) / 256;
     const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
     int cnt = 0, ntask = 0;
@@ -414,7 +417,6 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
     int o, to;
     const int total = block_exclusive_scan(cnt, &o, sh);
     const int ttotal = block_exclusive_scan(ntask, &to, sh);
-    const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
     for (int bk = b0; bk < b1; ++bk) {
       const int t = __ldcg(p.bucket_totals + bk);
       const int nt = (t + per_task - 1) / per_task;
@@ -442,6 +444,87 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
       p.counters[2] = min(ttotal, p.max_fwd_tasks);
       if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
     }
+  } else {
+    const int G = gridDim.x;
+    const int rper = (nb + G - 1) / G;  // buckets of each block's range
+    const int r0 = min(nb, blockIdx.x * rper), r1 = min(nb, r0 + rper);
+    // 3a. this block's range: its sums of entries and of work items
+    {
+      int cnt = 0, ntask = 0;
+      for (int bk = r0 + threadIdx.x; bk < r1; bk += blockDim.x) {
+        const int t = __ldcg(p.bucket_totals + bk);
+        cnt += t;
+        ntask += (t + per_task - 1) / per_task;
+      }
+      int unused;
+      const int rc = block_exclusive_scan(cnt, &unused, sh);
+      const int rt = block_exclusive_scan(ntask, &unused, sh);
+      if (threadIdx.x == 0) {
+        p.range_sums[blockIdx.x] = rc;
+        p.range_sums[G + blockIdx.x] = rt;
+      }
+    }
+    if (!grid_barrier(bar, p.status, &flag)) return;
+    // 3b. the ranges before this one give its first offset and first work item
+    {
+      int cnt = 0, ntask = 0, tot = 0, ttot = 0;
+      for (int b = threadIdx.x; b < G; b += blockDim.x) {
+        const int c = __ldcg(p.range_sums + b), t = __ldcg(p.range_sums + G + b);
+        tot += c;
+        ttot += t;
+        if (b < (int)blockIdx.x) {
+          cnt += c;
+          ntask += t;
+        }
+      }
+      int unused;
+      const int base = block_exclusive_scan(cnt, &unused, sh);
+      const int tbase = block_exclusive_scan(ntask, &unused, sh);
+      const int total = block_exclusive_scan(tot, &unused, sh);
+      const int ttotal = block_exclusive_scan(ttot, &unused, sh);
+      // the range's own scan: thread i takes buckets r0 + i per .. (a few each)
+      const int per = (r1 - r0 + (int)blockDim.x - 1) / (int)blockDim.x;
+      const int b0 = r0 + threadIdx.x * per, b1 = min(r1, b0 + per);
+      int c2 = 0, n2 = 0;
+      for (int bk = b0; bk < b1; ++bk) {
+        const int t = __ldcg(p.bucket_totals + bk);
+        c2 += t;
+        n2 += (t + per_task - 1) / per_task;
+      }
+      int o, to;
+      block_exclusive_scan(c2, &o, sh);
+      block_exclusive_scan(n2, &to, sh);
+      o += base;
+      to += tbase;
+      for (int bk = b0; bk < b1; ++bk) {
+        const int t = __ldcg(p.bucket_totals + bk);
+        const int nt = (t + per_task - 1) / per_task;
+        p.bucket_offsets[bk] = o;
+        for (int j = 0; j < nt; ++j) {
+          if (to + j < p.max_fwd_tasks) {
+            FwdTask ft;
+            ft.bucket = bk;
+            ft.entry_begin = o + j * per_task;
+            ft.count = min(per_task, t - j * per_task);
+            ft.pad = 0;
+            p.fwd_tasks[to + j] = ft;
+          }
+        }
+        o += t;
+        to += nt;
+      }
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        p.bucket_offsets[nb] = total;
+        if (total > p.max_entries) set_status(p.status, DEV_OVERFLOW);
+        p.counters[2] = min(ttotal, p.max_fwd_tasks);
+        if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
+      }
+    }
+    if (!grid_barrier(bar, p.status, &flag)) return;
+    // 3c. this block's own buckets' offsets, for the emit
+    if (ri)
+      for (int pg = threadIdx.x; pg < ri->npages; pg += blockDim.x)
+        s_boff[pg] = __ldcg(p.bucket_offsets + own0 + pg * p.Hkv);
   }
   __syncthreads();
   // ---- 4. emit

@@ -60,6 +60,8 @@ struct DevPlan {
   int32_t* chunk_offsets;   // [num_chunks + 1]: entries before each chunk
   int32_t* bucket_offsets;  // [num_buckets + 1]
   int32_t* bucket_totals;   // [num_buckets]: entries per bucket (single-launch inversion)
+  int32_t* range_sums;      // [2][inv_blocks]: entries and work items of each block's range of
+                            // buckets (single-launch inversion over many buckets)
   int2* entries;            // [max_entries] (row, t * 64 + slot), t = absolute position
   FwdTask* fwd_tasks;       // [max_fwd_tasks]
   // FP16 copies of quantised inputs (null when the plan has none), each rewritten by the call
