@@ -234,6 +234,8 @@ combine_kernel(int64_t rows, int32_t splits, const P* __restrict__ partial,
       if (!ok) break;
     }
   }
+  // a block exits only when all its threads have: the producer's copies land first
+  settle_after_abort(&sm.abort_flag);
 }
 
 template <typename P>

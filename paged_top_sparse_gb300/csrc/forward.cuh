@@ -646,6 +646,7 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       t = t2;
     }
   }
+  settle_after_abort(abort_flag);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -297,6 +297,7 @@ indexer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (!ok) break;
     }
   }
+  settle_after_abort(abort_flag);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

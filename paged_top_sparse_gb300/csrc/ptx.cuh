@@ -84,6 +84,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// After a role gave up (an abort), every thread of the block waits this long before the block
+// exits, so that copies its producers had already issued finish landing in its shared memory
+// (a copy takes microseconds); only the abort path pays it.  Placed before the kernel's final
+// block barrier, it holds the whole block back while the role that gave up waits.
+constexpr uint64_t kSettleNs = 200000ull;
+__device__ __forceinline__ void settle_after_abort(volatile int* abort) {
+  if (*abort) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
+  }
+}
+
 // Grid-wide barrier of a cooperative launch (every block resident).  Arrivals count up in
 // bar[0]; the last block resets it and advances the generation in bar[1], which the others
 // wait for.  The wait gives up after `limit_ns` (the library's wait limit), raising
