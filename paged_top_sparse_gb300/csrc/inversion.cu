@@ -402,7 +402,7 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
   // buckets (more than two per thread): each block sums its own range of buckets, a third grid
   // barrier, then each block scans the ranges' sums (one per block), writes its range's
   // offsets and work items, and after a fourth barrier reads its own buckets' offsets.
-  __shared__ int s_boff[512];  // CSR offset of page pg's bucket of this block's KV head
+  __shared__ int s_boff[kMaxPagesPerReq];  // CSR offset of page pg's bucket of this block's KV head
   const int nb = p.num_buckets;
   const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
   if (nb <= 2 * (int)blockDim.x) {

@@ -12,6 +12,8 @@ constexpr int kMaxTopK = 64;
 constexpr int kFwdTaskGroups = 8;  // 128-row query groups per forward work item
 constexpr int kChunkWords = 8;     // 32-row words per inversion chunk (one 256-thread block)
 constexpr int kInvPages = 64;      // pages per inversion window (one 64-bit row mask)
+constexpr int kMaxPagesPerReq = 1024;  // visible pages of one request (128K tokens): the top-k
+                                       // lane layouts and the inversion's offset table
 
 // One request of the batch, as the kernels see it.
 struct ReqInfo {

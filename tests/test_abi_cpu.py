@@ -89,11 +89,12 @@ def test_combine_validation_needs_no_device(L):
     assert b"split_stride" in L.sps_last_error()
 
 
-def test_plan_rejects_more_than_512_pages_per_request(L):
-    """The top-k lane layouts and the inversion windows are sized for at most 512 visible pages
-    (64K tokens of context per request); a plan beyond that is refused with a message."""
-    _plan(q_lens=[200], ctx_lens=[65300], max_pages_per_req=512, num_phys_pages=512)
+def test_plan_rejects_more_than_1024_pages_per_request(L):
+    """The top-k lane layouts and the inversion's offset table are sized for at most 1024
+    visible pages (128K tokens of context per request); a plan beyond that is refused with a
+    message naming the limit."""
+    _plan(q_lens=[200], ctx_lens=[130800], max_pages_per_req=1024, num_phys_pages=1024)
     with pytest.raises(B.SpsError) as e:
-        _plan(q_lens=[200], ctx_lens=[65400], max_pages_per_req=513, num_phys_pages=513)
+        _plan(q_lens=[200], ctx_lens=[130900], max_pages_per_req=1025, num_phys_pages=1025)
     assert e.value.status == 2
-    assert "512" in str(e.value)
+    assert "1024" in str(e.value)

@@ -54,9 +54,12 @@ def _workload(name):
         return synth.workload("custom", seed=16, q_lens=[190], ctx_lens=[70], num_q_heads=2,
                               num_kv_heads=1, head_dim=64, top_k=2, q_dtype="e4m3",
                               kv_dtype="nvfp4")
-    if name == "maxctx":  # the largest page count a plan takes (512 pages, 64K tokens)
+    if name == "maxctx":  # 512 pages, 64K tokens
         return synth.workload("custom", seed=41, q_lens=[200], ctx_lens=[65300], num_q_heads=4,
                               num_kv_heads=2, head_dim=128, top_k=16)
+    if name == "ctx128k":  # the largest page count a plan takes (1024 pages, 128K tokens)
+        return synth.workload("custom", seed=43, q_lens=[200], ctx_lens=[130800],
+                              num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=16)
     if name == "with_empty":  # requests without new tokens between others
         return synth.workload("custom", seed=42, q_lens=[0, 150, 0, 33],
                               ctx_lens=[500, 700, 0, 1000], num_q_heads=4, num_kv_heads=2,
@@ -69,7 +72,7 @@ def _workload(name):
 
 
 SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64",
-         "maxctx", "with_empty"]
+         "maxctx", "ctx128k", "with_empty"]
 FULL = ["prefill8k", "prefill8k_q", "chunked32k"]
 _cache = {}
 
@@ -155,6 +158,9 @@ def test_topk_bit_exact_on_shared_scores(name):
     ([300], [40000], 16),         # 315 pages
     ([100], [44000], 16),         # 345 pages
     ([50], [65000], 16),          # 508 pages
+    ([40], [89000], 16),          # 696 pages
+    ([30], [127900], 16),         # 1000 pages
+    ([20], [130900], 64),         # 1023 pages, the largest k
 ])
 def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     """Scores drawn from {-1.5, ..., 1.5} with signed zeros: most pages tie with others, so
