@@ -378,7 +378,9 @@ def run_prefill(args, world, dev, wname, partials="fp32", fp8qk=False, data=None
                    idx_k_dtype=idx_k, softmax_scale=w.sm_scale)
     plan = B.Plan(*plan_args, **plan_kw)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-    scores = torch.empty((R, w.max_pages), dtype=torch.float32, device=dev)
+    # row pitch a multiple of 4 floats (16-byte rows), as indexer_scores asks
+    pitch = (w.max_pages + 3) // 4 * 4
+    scores = torch.empty((R, pitch), dtype=torch.float32, device=dev)[:, : w.max_pages]
     idx = torch.empty((R, K), dtype=torch.int32, device=dev)
     p16 = partials != "fp32"  # 16-bit partial storage (BF16 or FP16)
     pdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[partials]

@@ -184,6 +184,9 @@ sps_status indexer_scores(const sps_plan* plan, const void* q_idx, float q_scale
  *           order, padded with -1 when the row sees fewer than top_k pages.
  * The own page o is always kept; the other min(top_k, o+1) - 1 are the best by (score
  * descending, page ascending), with -0.0 equal to +0.0.  NaN scores are outside the contract.
+ * Any score_pitch >= max_pages_per_req gives the same result; with top_k <= 16 a pitch that is
+ * a multiple of 4 on a 16-byte aligned buffer is the fast layout (the rows arrive by tensor
+ * copies), other pitches are read by per-thread loads.
  */
 sps_status topk_select(const sps_plan* plan, const float* scores, int64_t score_pitch,
                        int32_t* idx, void* workspace, sps_stream_t stream);

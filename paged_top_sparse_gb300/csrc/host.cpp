@@ -792,6 +792,21 @@ bool encode_tmap_3d(void* map, int dtype_code, void* base, uint64_t d0, uint64_t
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_2d_f32_sw64(void* map, const void* base, uint64_t inner, uint64_t outer,
+                             uint64_t outer_stride_bytes, uint32_t box_inner,
+                             uint32_t box_outer) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {outer_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   static int n = -1;
   if (n < 0) {

@@ -178,6 +178,10 @@ bool encode_tmap_2d(void* map, int dtype_code, void* base, uint64_t inner, uint6
 bool encode_tmap_3d(void* map, int dtype_code, void* base, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1,
                     uint32_t b2, bool swizzle128);
+// FP32 elements, 64-byte swizzle (box_inner * 4 == 64): the top-k score tiles.
+bool encode_tmap_2d_f32_sw64(void* map, const void* base, uint64_t inner, uint64_t outer,
+                             uint64_t outer_stride_bytes, uint32_t box_inner,
+                             uint32_t box_outer);
 int num_sms();
 
 }  // namespace sps

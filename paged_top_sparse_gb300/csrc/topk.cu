@@ -1,4 +1,4 @@
-// topk.cu -- per-row top-k page selection, one warp per row.
+// topk.cu -- per-row top-k page selection.
 //
 // Contract (the method's page selection: every row attends its own page, the one page the
 // forward of "MSA PR 21: Q8KV4 paged sparse prefill", K1 Softmax, masks causally; "MSA PR 36:
@@ -7,6 +7,20 @@
 // n_sel - 1 = min(k, o+1) - 1 pages are the best by (score descending, page ascending), with
 // -0.0 equal to +0.0; output in ascending page order, padded with -1.
 //
+// top_k <= 16: one thread per row.  The thread streams its row in groups of 16 pages and keeps
+// the 16 largest keys seen so far as a descending list: a group is sorted by Batcher's
+// odd-even merge network (63 comparators), the list takes the larger of list[i] and
+// group[15 - i] (a bitonic sequence that holds the 16 largest of both) and a bitonic merge
+// sorts it again.  The (k-1)-th largest key t then decides: every candidate above t is taken,
+// and of those equal to t the lowest pages fill the rest (the list's k-th entry shows whether
+// t is shared; the entries above t give how many equal ones are needed).  A second pass over
+// the row writes the chosen pages in ascending order into shared memory, and each warp stores
+// its 32 rows' outputs, which are contiguous, with coalesced stores.  Keys never carry page
+// numbers, so comparisons are plain unsigned min/max.  With 16-byte rows the scores reach
+// shared memory by TMA tile loads, one warp's 32 rows x 16 pages per tile (topk_tma_kernel);
+// other layouts are read by per-thread loads (topk_thread_kernel).
+//
+// Larger top_k (the warp kernels below): one warp per row.
 // Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
 // sorted best-first once (bitonic network in registers), so any page of a lower lane is lower
 // than every page of a higher lane.  A selection round is then one warp max-reduction
@@ -30,6 +44,363 @@ namespace {
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The float a key was made from (+0.0 for the key of either zero).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+__device__ __forceinline__ void cmpx_desc(uint32_t& a, uint32_t& b) {  // a <- max, b <- min
+  const uint32_t hi = max(a, b);
+  b = min(a, b);
+  a = hi;
+}
+
+// Sorts 16 keys in descending order: Batcher's odd-even merge sort (K. E. Batcher, "Sorting
+// networks and their applications", AFIPS 1968), 63 comparators in its ten layers, written
+// out so that every index is a constant.
+__device__ __forceinline__ void sort16_desc(uint32_t (&x)[16]) {
+#define C(a, b) cmpx_desc(x[a], x[b])
+  C(0, 1); C(2, 3); C(4, 5); C(6, 7); C(8, 9); C(10, 11); C(12, 13); C(14, 15);
+  C(0, 2); C(1, 3); C(4, 6); C(5, 7); C(8, 10); C(9, 11); C(12, 14); C(13, 15);
+  C(1, 2); C(5, 6); C(9, 10); C(13, 14);
+  C(0, 4); C(1, 5); C(2, 6); C(3, 7); C(8, 12); C(9, 13); C(10, 14); C(11, 15);
+  C(2, 4); C(3, 5); C(10, 12); C(11, 13);
+  C(1, 2); C(3, 4); C(5, 6); C(9, 10); C(11, 12); C(13, 14);
+  C(0, 8); C(1, 9); C(2, 10); C(3, 11); C(4, 12); C(5, 13); C(6, 14); C(7, 15);
+  C(4, 8); C(5, 9); C(6, 10); C(7, 11);
+  C(2, 4); C(3, 5); C(6, 8); C(7, 9); C(10, 12); C(11, 13);
+  C(1, 2); C(3, 4); C(5, 6); C(7, 8); C(9, 10); C(11, 12); C(13, 14);
+#undef C
+}
+
+// best <- the 16 largest of best and g (both descending), descending.
+__device__ __forceinline__ void merge16_desc(uint32_t (&best)[16], const uint32_t (&g)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) best[i] = max(best[i], g[15 - i]);
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & s) == 0) cmpx_desc(best[i], best[i + s]);
+}
+
+// Scores of pages c .. c+3 (c < o); entries of pages at or past o are unspecified.  VEC: the
+// row is 16-byte aligned and its pitch a multiple of 4, so the four floats lie inside the row.
+template <bool VEC>
+__device__ __forceinline__ float4 load4_raw(const float* row, int c, int o) {
+  if (VEC) return __ldg(reinterpret_cast<const float4*>(row + c));
+  float4 f;
+  f.x = __ldg(row + c);
+  f.y = c + 1 < o ? __ldg(row + c + 1) : 0.f;
+  f.z = c + 2 < o ? __ldg(row + c + 2) : 0.f;
+  f.w = c + 3 < o ? __ldg(row + c + 3) : 0.f;
+  return f;
+}
+
+// The 16 scores of pages base .. base+15 (base < o) as four float4; entries of pages at or past
+// o are unspecified.  All loads are issued before any is used.
+template <bool VEC>
+__device__ __forceinline__ void load_group(const float* row, int base, int o, float4 (&f)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    f[q] = base + 4 * q < o ? load4_raw<VEC>(row, base + 4 * q, o) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Pass 1 of a row: the keys of pages base .. base+15 that lie below o join the running list
+// of the 16 largest.
+__device__ __forceinline__ void take_group(uint32_t (&best)[16], const float4 (&f)[4], int base,
+                                           int o) {
+  uint32_t g[16];
+  if (base + 16 <= o) {  // a full group: every page is a candidate
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      g[4 * q + 0] = score_key(f[q].x);
+      g[4 * q + 1] = score_key(f[q].y);
+      g[4 * q + 2] = score_key(f[q].z);
+      g[4 * q + 3] = score_key(f[q].w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = base + 4 * q;
+      g[4 * q + 0] = c + 0 < o ? score_key(f[q].x) : 0u;
+      g[4 * q + 1] = c + 1 < o ? score_key(f[q].y) : 0u;
+      g[4 * q + 2] = c + 2 < o ? score_key(f[q].z) : 0u;
+      g[4 * q + 3] = c + 3 < o ? score_key(f[q].w) : 0u;
+    }
+  }
+  sort16_desc(g);
+  merge16_desc(best, g);
+}
+
+// The selection rule read off the list (o >= K >= 2 candidates, so the (K-1)-th and K-th
+// largest keys both exist), t being the (K-1)-th largest key.  When the K-th key differs from t,
+// the chosen candidates are exactly those with score >= t's score.  When it equals t (shared),
+// every candidate above t is taken and `need` of those equal to it, the lowest pages first.
+struct TopkRule {
+  float ge;  // while need == 0 the pages with score >= ge are taken
+  float eq;  // t's score: with need > 0, pages above it and `need` more equal to it are taken
+  int need;
+};
+
+__device__ __forceinline__ TopkRule selection_rule(const uint32_t (&best)[16], int K) {
+  // the list is descending: t = best[K-2] is the least of the first K-1 entries, t_next =
+  // best[K-1] the largest of the rest (reductions, so that no entry is picked by a run-time index)
+  uint32_t t = 0xffffffffu, t_next = 0u;
+  int above = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    t = i < K - 1 ? min(t, best[i]) : t;
+    t_next = i >= K - 1 ? max(t_next, best[i]) : t_next;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) above += best[i] > t ? 1 : 0;
+  TopkRule rule;
+  const bool shared = t_next == t;
+  rule.eq = key_score(t);
+  // shared: once the equal pages are in, the threshold is the least score above t's (the key
+  // order is the score order, so that is the score of key t + 1)
+  rule.ge = shared ? key_score(t + 1u) : rule.eq;
+  rule.need = shared ? K - 1 - above : 0;
+  return rule;
+}
+
+// Pass 2 of a row: the chosen pages among base .. base+15 (those below o), in ascending order,
+// into the row's staging so[pos ...].  While no equal page is still needed the group becomes a
+// 16-bit mask of the taken pages, walked lowest bit first; otherwise page by page.  pos is
+// masked by 15: the staging row stays in bounds whatever the scores.
+__device__ __forceinline__ void emit_group(const float4 (&f)[4], int base, int o, TopkRule& rule,
+                                           int32_t* so, int& pos) {
+  float v[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[4 * q + 0] = f[q].x;
+    v[4 * q + 1] = f[q].y;
+    v[4 * q + 2] = f[q].z;
+    v[4 * q + 3] = f[q].w;
+  }
+  const int nb = o - base < 16 ? o - base : 16;  // candidate pages in the group
+  if (rule.need == 0) {
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) bits |= v[e] >= rule.ge ? 1u << e : 0u;
+    if (nb < 16) bits &= (1u << nb) - 1u;
+    while (bits) {
+      so[pos++ & 15] = base + __ffs(bits) - 1;
+      bits &= bits - 1u;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      if (e >= nb) break;
+      const bool eq = v[e] == rule.eq && rule.need > 0;
+      if (v[e] > rule.eq || eq) so[pos++ & 15] = base + e;
+      rule.need -= eq ? 1 : 0;
+    }
+  }
+}
+
+// The rows that keep every visible page (o < K), and K = 1 (the own page alone).
+__device__ __forceinline__ void stage_short_row(int32_t* so, int o, int K) {
+  if (K == 1) {
+    so[0] = o;
+  } else {
+    for (int s = 0; s < K; ++s) so[s] = s <= o ? s : -1;
+  }
+}
+
+// A warp's 32 rows are consecutive, so their outputs are one contiguous run of nrow * K ints;
+// the warp stores it from the staging rows (pitch OP) with coalesced stores.
+template <int OP>
+__device__ __forceinline__ void store_staged(const int32_t* s_warp, int32_t* dst, int nrow, int K,
+                                             int lane) {
+  const int dr = 32 / K, dc = 32 % K;
+  int row = lane / K, col = lane % K;
+  for (int w = lane; w < nrow * K; w += 32) {
+    dst[w] = s_warp[row * OP + col];
+    row += dr;
+    col += dc;
+    if (col >= K) {
+      col -= K;
+      ++row;
+    }
+  }
+}
+
+constexpr int kTopkOP = 17;  // staging row pitch (ints): conflict-free per-thread writes
+
+// top_k <= 16, any row pitch: every thread loads its own row (VEC: 16-byte loads).
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+topk_thread_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
+                   int32_t* __restrict__ idx) {
+  __shared__ int32_t s_out[256 * kTopkOP];
+  pdl_wait();  // the scores come from the indexer just before
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t R = (int64_t)p.T * p.H;
+  const int64_t r0 = (int64_t)blockIdx.x * 256 + warp * 32;  // the warp's first row
+  if (r0 >= R) return;                                       // warp-uniform
+  const int64_t r = r0 + lane;
+  const int K = p.K;
+  int32_t* so = s_out + threadIdx.x * kTopkOP;
+  if (r < R) {
+    // own page o; the pages 0 .. o-1 are the candidates
+    const int o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
+    if (o < K || K == 1) {
+      stage_short_row(so, o, K);
+    } else {
+      const float* row = scores + r * pitch;
+      uint32_t best[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) best[i] = 0u;
+      float4 f[4];
+      load_group<VEC>(row, 0, o, f);
+      for (int base = 0; base < o; base += 16) {
+        float4 cur[4] = {f[0], f[1], f[2], f[3]};
+        if (base + 16 < o) load_group<VEC>(row, base + 16, o, f);  // in flight meanwhile
+        take_group(best, cur, base, o);
+      }
+      TopkRule rule = selection_rule(best, K);
+      int pos = 0;
+      load_group<VEC>(row, 0, o, f);
+      for (int base = 0; base < o; base += 16) {
+        float4 cur[4] = {f[0], f[1], f[2], f[3]};
+        if (base + 16 < o) load_group<VEC>(row, base + 16, o, f);
+        emit_group(cur, base, o, rule, so, pos);
+      }
+      so[K - 1] = o;  // the own page is the row's last visible page
+    }
+  }
+  __syncwarp();
+  const int nrow = R - r0 < 32 ? (int)(R - r0) : 32;
+  store_staged<kTopkOP>(s_out + warp * 32 * kTopkOP, idx + r0 * K, nrow, K, lane);
+}
+
+// top_k <= 16, row pitch a multiple of 4 floats, at least 16 pages and 32 rows: the same
+// per-row work, with each warp's 32 rows x 16 scores brought into shared memory by one TMA
+// tile load (64-byte swizzle: the 16-byte chunk c of tile row t sits at chunk c ^ ((t >> 1) & 3),
+// so the 32 threads' reads of their own rows hit distinct banks).  Each warp runs its own ring
+// of S tiles: its pass 1 over groups 0 .. G-1 and its pass 2 over them again are one sequence
+// of 2G tile loads, issued S ahead by lane 0.  G is the largest group count of the warp's rows.  Waits are bounded; a warp that gives up raises DEV_TIMEOUT and leaves
+// its rows unwritten.
+constexpr int kTopkTile = 32 * 16 * 4;  // bytes of one tile
+template <int S>
+constexpr size_t topk_smem() {
+  return 1024 + 8 * S * kTopkTile + 8 * S * 8 + 256 * kTopkOP * 4;
+}
+
+// Lane 0 of a warp: the tile load of item n of its sequence (group n, or n - G in pass 2)
+// into stage n % S.
+template <int S>
+__device__ __forceinline__ void topk_issue_tile(const CUtensorMap* tm, uint32_t tiles,
+                                                uint32_t bars, int n, int G, int r0) {
+  const int s = n % S;
+  mbar_expect_tx(bars + 8 * s, kTopkTile);
+  tma_load_2d(tiles + s * kTopkTile, tm, 16 * (n < G ? n : n - G), r0, bars + 8 * s);
+}
+
+// Every lane waits for item n's tile (stage n % S); true on all lanes when it landed.
+template <int S>
+__device__ __forceinline__ bool topk_tile_ready(uint32_t bar, int n, int32_t* status) {
+  const bool got = mbar_wait(bar, (uint32_t)(n / S) & 1u, nullptr, status);
+  return __all_sync(0xffffffffu, got);
+}
+
+// This lane's row (tile row `lane`) of a landed tile: chunk c at 16 (c ^ ((lane >> 1) & 3)).
+__device__ __forceinline__ void topk_read_tile(const uint8_t* tile, int lane, float4 (&f)[4]) {
+  const uint8_t* row = tile + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) f[c] = *reinterpret_cast<const float4*>(row + 16 * (c ^ sw));
+}
+
+template <int S>
+__global__ void __launch_bounds__(256)
+topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + 8 * S * kTopkTile);
+  int32_t* s_out = reinterpret_cast<int32_t*>(bars + 8 * S);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t my_tiles = smem_u32(tiles + warp * S * kTopkTile);
+  const uint32_t my_bars = smem_u32(bars + warp * S);
+  if (lane == 0) {
+    tma_prefetch_desc(&tmS);
+    for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_wait();  // the scores come from the indexer just before
+  const int64_t R = (int64_t)p.T * p.H;
+  const int64_t r0 = (int64_t)blockIdx.x * 256 + warp * 32;
+  if (r0 >= R) return;  // warp-uniform; this warp issued no copy
+  const int64_t r = r0 + lane;
+  const int K = p.K;
+  int32_t* so = s_out + threadIdx.x * kTopkOP;
+  int o = 0;
+  bool full = false;  // the row runs both passes
+  if (r < R) {
+    o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
+    full = o >= K && K > 1;
+    if (!full) stage_short_row(so, o, K);
+  }
+  const int G = (int)__reduce_max_sync(0xffffffffu, full ? (uint32_t)(o + 15) / 16u : 0u);
+  const int items = 2 * G;
+  if (lane == 0)
+    for (int n = 0; n < S && n < items; ++n)
+      topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
+  uint32_t best[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) best[i] = 0u;
+  TopkRule rule{};
+  bool ok = true;
+  int pos = 0;
+  // pass 1: groups 0 .. G-1 into the running list
+  int n = 0;
+  for (; n < G; ++n) {
+    const int s = n % S;
+    if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
+      ok = false;
+      break;
+    }
+    if (full && 16 * n < o) {
+      float4 f[4];
+      topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
+      take_group(best, f, 16 * n, o);
+    }
+    __syncwarp();  // every lane is done with stage s
+    if (lane == 0 && n + S < items)
+      topk_issue_tile<S>(&tmS, my_tiles, my_bars, n + S, G, (int)r0);
+  }
+  if (full) rule = selection_rule(best, K);
+  // pass 2: the same groups again, the chosen pages in ascending order
+  for (; ok && n < items; ++n) {
+    const int s = n % S;
+    if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
+      ok = false;
+      break;
+    }
+    if (full && 16 * (n - G) < o) {
+      float4 f[4];
+      topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
+      emit_group(f, 16 * (n - G), o, rule, so, pos);
+    }
+    __syncwarp();
+    if (lane == 0 && n + S < items)
+      topk_issue_tile<S>(&tmS, my_tiles, my_bars, n + S, G, (int)r0);
+  }
+  if (!ok) {  // let the copies already issued land before the block's shared memory is reused
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
+    return;
+  }
+  if (full) so[K - 1] = o;  // the own page is the row's last visible page
+  __syncwarp();
+  const int nrow = R - r0 < 32 ? (int)(R - r0) : 32;
+  store_staged<kTopkOP>(s_out + warp * 32 * kTopkOP, idx + r0 * K, nrow, K, lane);
 }
 
 // Sorts a lane's E candidates (key, page offset) best-first: larger key, then lower page.
@@ -265,24 +636,46 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
 
 }  // namespace
 
+template <int S>
+cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, int32_t* idx, unsigned grid,
+                            cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(topk_tma_kernel<S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)topk_smem<S>());
+  if (e != cudaSuccess) return e;
+  return launch_pdl(topk_tma_kernel<S>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p, idx);
+}
+
 cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, int32_t* idx,
                         cudaStream_t st) {
   const int64_t R = (int64_t)p.T * p.H;
-  const unsigned grid = (unsigned)((R + 7) / 8);
-  if (grid == 0) return cudaSuccess;
-  // top_k = 16 (the common case) runs instances whose rounds unroll completely (the filtered
-  // long rows do better with the rolled loop)
-  const bool k16 = p.K == 16;
+  if (R == 0) return cudaSuccess;
   cudaError_t e;
+  if (p.K <= 16) {
+    const unsigned grid = (unsigned)((R + 255) / 256);
+    const bool vec = pitch % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
+    alignas(64) CUtensorMap tm;
+    if (vec && p.max_pages >= 16 && R >= 32 &&
+        encode_tmap_2d_f32_sw64(&tm, scores, (uint64_t)p.max_pages, (uint64_t)R,
+                                (uint64_t)pitch * 4, 16, 32)) {
+      // rows of many groups need a deeper ring per warp to cover the tile latency (4 stages: two
+      // blocks per SM); short rows do better with three blocks per SM (3 stages)
+      if (p.max_pages <= 128) e = launch_topk_tma<3>(tm, p, idx, grid, st);
+      else e = launch_topk_tma<4>(tm, p, idx, grid, st);
+    } else if (vec) {
+      e = launch_pdl(topk_thread_kernel<true>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    } else {
+      e = launch_pdl(topk_thread_kernel<false>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  const unsigned grid = (unsigned)((R + 7) / 8);
   if (p.max_pages <= 32) {
-    if (k16) e = launch_pdl(topk_kernel<1, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
-    else e = launch_pdl(topk_kernel<1>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    e = launch_pdl(topk_kernel<1>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 64) {
-    if (k16) e = launch_pdl(topk_kernel<2, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
-    else e = launch_pdl(topk_kernel<2>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    e = launch_pdl(topk_kernel<2>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 128) {
-    if (k16) e = launch_pdl(topk_kernel<4, 16>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
-    else e = launch_pdl(topk_kernel<4>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
+    e = launch_pdl(topk_kernel<4>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 256) {
     e = launch_pdl(topk_filter_kernel<8, 8>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else if (p.max_pages <= 320) {

@@ -45,7 +45,7 @@ class DeviceRun:
         self.ws = torch.zeros(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
         B.sps_plan_upload(self.plan, self.ws)
         R, K, D = w.num_rows, w.top_k, w.head_dim
-        self.pitch = pitch or w.max_pages
+        self.pitch = pitch or (w.max_pages + 3) // 4 * 4  # 16-byte rows, as the header asks
         self.scores = torch.full((R, self.pitch), float("nan"), dtype=torch.float32, device=dev)
         self.idx = torch.full((R, K), -7, dtype=torch.int32, device=dev)
         self.partial = torch.full((K, R, D), float("nan"), dtype=torch.float32, device=dev)

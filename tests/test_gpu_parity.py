@@ -188,6 +188,49 @@ def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     assert np.array_equal(idx.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("pad", [0, 1, 4])
+@pytest.mark.parametrize("q_lens,ctx_lens,k", [
+    ([150, 90, 301], [2100, 700, 0], 16),  # three requests: rows of a warp see different pages
+    ([200], [7000], 15),
+    ([100], [9000], 2),
+    ([120], [5000], 1),
+    ([64], [40000], 16),                   # 313 pages: twenty groups of 16
+])
+def test_topk_strided_scores(q_lens, ctx_lens, k, pad):
+    """The score buffer as a view whose row pitch exceeds max_pages (pad 0 and 4: a pitch that
+    is a multiple of 4, read with 16-byte loads; pad 1: an odd pitch, read element by element).
+    Half the rows hold N(0,1) scores, half scores from {-1, -0.5, 0, 0.5, 1} (ties); every entry
+    past the own page and the pitch padding hold NaN."""
+    from paged_top_sparse_gb300 import binding as B
+
+    w = synth.workload("custom", seed=22, q_lens=q_lens, ctx_lens=ctx_lens, num_q_heads=4,
+                       num_kv_heads=2, head_dim=128, top_k=k)
+    plan = B.Plan(w.q_lens, w.ctx_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.top_k,
+                  w.max_pages, w.num_phys_pages)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda:0")
+    B.sps_plan_upload(plan, ws)
+    rng = np.random.default_rng(6)
+    R, P = w.num_rows, w.max_pages
+    s = rng.standard_normal((R, P)).astype(np.float32)
+    tie_rows = rng.random(R) < 0.5
+    s[tie_rows] = (rng.integers(-2, 3, size=(int(tie_rows.sum()), P)) * 0.5).astype(np.float32)
+    _, tok_pos = orc.token_meta(oracle_problem(w))
+    own = (tok_pos[np.arange(R) // w.num_q_heads] // 128)[:, None]
+    s[np.arange(P)[None, :] > own] = np.nan
+    pitch = (P + 3) // 4 * 4 + pad
+    buf = torch.full((R, pitch), float("nan"), dtype=torch.float32, device="cuda:0")
+    buf[:, :P] = torch.from_numpy(s).cuda()
+    view = buf[:, :P]
+    assert view.stride(0) == pitch
+    idx = torch.full((R, k), -7, dtype=torch.int32, device="cuda:0")
+    B.topk_select(plan, view, idx, ws)
+    torch.cuda.synchronize()
+    ref = orc.topk(oracle_problem(w), np.nan_to_num(s.astype(np.float64), nan=-np.inf))
+    got = idx.cpu().numpy()
+    bad = np.nonzero(~np.all(got == ref, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
+
+
 @pytest.mark.parametrize("name", SMALL + FULL)
 def test_forward_partials_and_lse(name):
     r = _run(name)
