@@ -114,75 +114,6 @@ struct RowSel {
   }
 };
 
-// The row's valid selections in pages [p0, p0 + 64) as a bit mask (bit d: page p0 + d).
-template <int KV>
-__device__ __forceinline__ uint64_t row_mask(const RowSel<KV>& sel, const RowCtx& rc, int p0) {
-  uint64_t m = 0;
-  if (rc.valid) {
-#pragma unroll
-    for (int s = 0; s < sel.n(); ++s) {
-      const int pg = sel.get(s);
-      const int d = pg - p0;
-      if (d >= 0 && d < kInvPages && pg <= rc.o) m |= 1ull << d;
-    }
-  }
-  return m;
-}
-
-// Turns the warp's 32 row masks around into one 32-row mask per page: tm[d][warp] bit l set
-// when row l of the warp selected page p0 + d.
-__device__ __forceinline__ void masks_to_smem(uint32_t (*tm)[kChunkWords + 1], uint64_t m, int warp,
-                                              int lane) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t b0 = __ballot_sync(0xffffffffu, (uint32_t)(m >> j) & 1u);
-    const uint32_t b1 = __ballot_sync(0xffffffffu, (uint32_t)(m >> (j + 32)) & 1u);
-    if (lane == j) {
-      lo = b0;
-      hi = b1;
-    }
-  }
-  tm[lane][warp] = lo;
-  tm[lane + 32][warp] = hi;
-}
-
-template <int KV>
-__global__ void __launch_bounds__(256, 8)
-count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
-             int64_t lse_split_stride) {
-  __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
-  int g, c;
-  const int b = find_block(p, blockIdx.x, &g, &c);
-  if (b < 0) return;  // uniform over the block
-  const ReqInfo& ri = p.reqs[b];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
-  RowSel<KV> sel;
-  sel.load(idx, rc, p.K);
-  if (rc.valid) {
-#pragma unroll
-    for (int s = 0; s < sel.n(); ++s) {
-      if (s >= p.K) break;
-      const int pg = sel.get(s);
-      if (pg < 0) lse[s * lse_split_stride + rc.r] = -INFINITY;
-      else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
-    }
-  }
-  for (int p0 = 0; p0 < ri.npages; p0 += kInvPages) {
-    masks_to_smem(tm, row_mask(sel, rc, p0), warp, lane);
-    __syncthreads();
-    const int d = threadIdx.x;
-    if (d < kInvPages && p0 + d < ri.npages) {
-      int n = 0;
-#pragma unroll 8
-      for (int v = 0; v < kChunkWords; ++v) n += __popc(tm[d][v]);
-      p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)] = n;  // a count until step 2
-    }
-    __syncthreads();
-  }
-}
-
 // Block-wide exclusive scan of one int per thread; returns the block total.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* out, int* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -208,6 +139,102 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* out, int* sh) {
   *out = (warp ? sh[warp - 1] : 0) + x - v;
   __syncthreads();
   return total;
+}
+
+static_assert(kChunkWords * 32 == 256, "a chunk is one 256-thread block, a warp per 32 rows");
+
+// The row's valid selections in pages [p0, p0 + 64) as a bit mask (bit d: page p0 + d).
+template <int KV>
+__device__ __forceinline__ uint64_t row_mask(const RowSel<KV>& sel, const RowCtx& rc, int p0) {
+  uint64_t m = 0;
+  if (rc.valid) {
+#pragma unroll
+    for (int s = 0; s < sel.n(); ++s) {
+      const int pg = sel.get(s);
+      const int d = pg - p0;
+      if (d >= 0 && d < kInvPages && pg <= rc.o) m |= 1ull << d;
+    }
+  }
+  return m;
+}
+
+// Page masks of the block's rows for the windows w0 <= w < w1: tm[w - w0][d][v] bit l is set
+// when row l of warp v selected page 64 w + d.  One window: each warp turns its 32 row masks
+// around with 64 ballots.  Several: the masks are cleared and every selection ORs its lane's
+// bit into its page's word (a row has at most top_k selections, while the ballots cost 64 per
+// window; with one window the ballots win, since many lanes of a warp share pages, the own
+// page above all, and their ORs to one word serialise).  Every thread of the block calls it.
+template <int KV>
+__device__ __forceinline__ void build_masks(uint32_t (*tm)[kInvPages][kChunkWords + 1], int w0,
+                                            int w1, const RowSel<KV>& sel, const RowCtx& rc,
+                                            int warp, int lane) {
+  if (w1 - w0 == 1) {
+    const uint64_t m = row_mask(sel, rc, w0 * kInvPages);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t b0 = __ballot_sync(0xffffffffu, (uint32_t)(m >> j) & 1u);
+      const uint32_t b1 = __ballot_sync(0xffffffffu, (uint32_t)(m >> (j + 32)) & 1u);
+      if (lane == j) {
+        lo = b0;
+        hi = b1;
+      }
+    }
+    tm[0][lane][warp] = lo;
+    tm[0][lane + 32][warp] = hi;
+    __syncthreads();
+    return;
+  }
+  uint32_t* flat = &tm[0][0][0];
+  const int n = (w1 - w0) * kInvPages * (kChunkWords + 1);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) flat[i] = 0u;
+  __syncthreads();
+  if (rc.valid) {
+#pragma unroll
+    for (int s = 0; s < sel.n(); ++s) {
+      const int pg = sel.get(s);
+      if (pg < 0 || pg > rc.o) continue;
+      const int w = pg / kInvPages;
+      if (w < w0 || w >= w1) continue;
+      atomicOr(&tm[w - w0][pg % kInvPages][warp], 1u << lane);
+    }
+  }
+  __syncthreads();
+}
+
+template <int KV>
+__global__ void __launch_bounds__(256, 8)
+count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
+             int64_t lse_split_stride) {
+  __shared__ uint32_t tm[1][kInvPages][kChunkWords + 1];
+  int g, c;
+  const int b = find_block(p, blockIdx.x, &g, &c);
+  if (b < 0) return;  // uniform over the block
+  const ReqInfo& ri = p.reqs[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
+  RowSel<KV> sel;
+  sel.load(idx, rc, p.K);
+  if (rc.valid) {
+#pragma unroll
+    for (int s = 0; s < sel.n(); ++s) {
+      if (s >= p.K) break;
+      const int pg = sel.get(s);
+      if (pg < 0) lse[s * lse_split_stride + rc.r] = -INFINITY;
+      else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
+    }
+  }
+  for (int wi = 0; wi * kInvPages < ri.npages; ++wi) {
+    build_masks(tm, wi, wi + 1, sel, rc, warp, lane);
+    const int d = threadIdx.x, p0 = wi * kInvPages;
+    if (d < kInvPages && p0 + d < ri.npages) {
+      int n = 0;
+#pragma unroll 8
+      for (int v = 0; v < kChunkWords; ++v) n += __popc(tm[0][d][v]);
+      p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)] = n;  // a count until step 2
+    }
+    __syncthreads();
+  }
 }
 
 // Step 3 (one block): bucket totals -> CSR offsets (in place), then the forward's work list.
@@ -286,7 +313,7 @@ __global__ void __launch_bounds__(256) scan_kernel(DevPlan p) {
 template <int KV>
 __global__ void __launch_bounds__(256, 8)
 emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
-  __shared__ uint32_t tm[kInvPages][kChunkWords + 1];
+  __shared__ uint32_t tm[1][kInvPages][kChunkWords + 1];
   __shared__ int pos0[kInvPages][kChunkWords + 1];  // first entry of (page, warp)
   pdl_trigger();  // the forward that follows may start its prologue
   int g, c;
@@ -299,15 +326,14 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   sel.load(idx, rc, p.K);
   const uint32_t below = (1u << lane) - 1u;
   for (int p0 = 0; p0 < ri.npages; p0 += kInvPages) {
-    masks_to_smem(tm, row_mask(sel, rc, p0), warp, lane);
-    __syncthreads();
+    build_masks(tm, p0 / kInvPages, p0 / kInvPages + 1, sel, rc, warp, lane);
     const int d = threadIdx.x;
     if (d < kInvPages && p0 + d < ri.npages) {
       const int bk = (ri.page_base + p0 + d) * p.Hkv + g;
       int acc = p.bucket_offsets[bk] + p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)];
       for (int v = 0; v < kChunkWords; ++v) {
         pos0[d][v] = acc;
-        acc += __popc(tm[d][v]);
+        acc += __popc(tm[0][d][v]);
       }
     }
     __syncthreads();
@@ -317,7 +343,7 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
         const int pg = sel.get(s);
         const int dd = pg - p0;
         if (dd < 0 || dd >= kInvPages || pg > rc.o) continue;
-        const int pos = pos0[dd][warp] + __popc(tm[dd][warp] & below);
+        const int pos = pos0[dd][warp] + __popc(tm[0][dd][warp] & below);
         p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
       }
     }
@@ -337,7 +363,9 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
   extern __shared__ uint32_t dyn[];
   uint32_t (*tmw)[kInvPages][kChunkWords + 1] =
       reinterpret_cast<uint32_t (*)[kInvPages][kChunkWords + 1]>(dyn);  // [nwin]
-  __shared__ int pos0[kInvPages][kChunkWords + 1];
+  int (*pos0)[kInvPages][kChunkWords + 1] =  // [nwin]: first entry of (page, warp)
+      reinterpret_cast<int (*)[kInvPages][kChunkWords + 1]>(
+          dyn + (size_t)nwin * kInvPages * (kChunkWords + 1));
   __shared__ int sh[32];
   __shared__ int flag;
   unsigned int* bar = reinterpret_cast<unsigned int*>(p.counters + 4);
@@ -362,9 +390,7 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
         else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
       }
     }
-    for (int wi = 0; wi * kInvPages < ri->npages; ++wi)
-      masks_to_smem(tmw[wi], row_mask(sel, rc, wi * kInvPages), warp, lane);
-    __syncthreads();
+    build_masks(tmw, 0, (ri->npages + kInvPages - 1) / kInvPages, sel, rc, warp, lane);
     for (int wi = 0; wi * kInvPages < ri->npages; ++wi) {
       const int d = threadIdx.x, p0 = wi * kInvPages;
       if (d < kInvPages && p0 + d < ri->npages) {
@@ -527,30 +553,28 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
         s_boff[pg] = __ldcg(p.bucket_offsets + own0 + pg * p.Hkv);
   }
   __syncthreads();
-  // ---- 4. emit
+  // ---- 4. emit: every (page, warp) start of the request's windows in one pass, then each
+  // selection's entry
   if (!ri) return;
-  const uint32_t below = (1u << lane) - 1u;
-  for (int wi = 0; wi * kInvPages < ri->npages; ++wi) {
-    const int d = threadIdx.x, p0 = wi * kInvPages;
-    if (d < kInvPages && p0 + d < ri->npages) {
-      int acc = s_boff[p0 + d] + __ldcg(p.chunk_offsets + chunk_id(p, *ri, p0 + d, g, c));
-      for (int v = 0; v < kChunkWords; ++v) {
-        pos0[d][v] = acc;
-        acc += __popc(tmw[wi][d][v]);
-      }
+  for (int pg = threadIdx.x; pg < ri->npages; pg += blockDim.x) {
+    const int wi = pg / kInvPages, d = pg % kInvPages;
+    int acc = s_boff[pg] + __ldcg(p.chunk_offsets + chunk_id(p, *ri, pg, g, c));
+    for (int v = 0; v < kChunkWords; ++v) {
+      pos0[wi][d][v] = acc;
+      acc += __popc(tmw[wi][d][v]);
     }
-    __syncthreads();
-    if (rc.valid) {
+  }
+  __syncthreads();
+  if (rc.valid) {
+    const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
-      for (int s = 0; s < sel.n(); ++s) {
-        const int pg = sel.get(s);
-        const int dd = pg - p0;
-        if (dd < 0 || dd >= kInvPages || pg > rc.o) continue;
-        const int pos = pos0[dd][warp] + __popc(tmw[wi][dd][warp] & below);
-        p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
-      }
+    for (int s = 0; s < sel.n(); ++s) {
+      const int pg = sel.get(s);
+      if (pg < 0 || pg > rc.o) continue;
+      const int wi = pg / kInvPages, d = pg % kInvPages;
+      const int pos = pos0[wi][d][warp] + __popc(tmw[wi][d][warp] & below);
+      p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
     }
-    __syncthreads();
   }
 }
 
@@ -559,7 +583,7 @@ bool try_fused(const DevPlan& p, const int32_t* idx, float* lse, int64_t lse_spl
                cudaStream_t st, cudaError_t* err) {
   // max_pages bounds every request's page count, so it sizes the 64-page windows
   const int nwin = (p.max_pages + kInvPages - 1) / kInvPages;
-  const size_t dsmem = (size_t)nwin * kInvPages * (kChunkWords + 1) * sizeof(uint32_t);
+  const size_t dsmem = (size_t)2 * nwin * kInvPages * (kChunkWords + 1) * sizeof(uint32_t);
   auto kern = fused_kernel<KV>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, dsmem) != cudaSuccess) {
