@@ -8,17 +8,19 @@
 // -0.0 equal to +0.0; output in ascending page order, padded with -1.
 //
 // top_k <= 16: one thread per row.  The thread streams its row in groups of 16 pages and keeps
-// the 16 largest keys seen so far as a descending list: a group is sorted by Batcher's
+// the 16 largest scores seen so far as a descending list: a group is sorted by Batcher's
 // odd-even merge network (63 comparators), the list takes the larger of list[i] and
 // group[15 - i] (a bitonic sequence that holds the 16 largest of both) and a bitonic merge
-// sorts it again.  The (k-1)-th largest key t then decides: every candidate above t is taken,
+// sorts it again.  The (k-1)-th largest score t then decides: every candidate above t is taken,
 // and of those equal to t the lowest pages fill the rest (the list's k-th entry shows whether
 // t is shared; the entries above t give how many equal ones are needed).  A second pass over
 // the row writes the chosen pages in ascending order into shared memory, and each warp stores
-// its 32 rows' outputs, which are contiguous, with coalesced stores.  Keys never carry page
-// numbers, so comparisons are plain unsigned min/max.  With 16-byte rows the scores reach
-// shared memory by TMA tile loads, one warp's 32 rows x 16 pages per tile (topk_tma_kernel);
-// other layouts are read by per-thread loads (topk_thread_kernel).
+// its 32 rows' outputs, which are contiguous, with coalesced stores.  The list never carries
+// page numbers, so the network is plain FP32 min/max on the scores themselves: -0.0 and +0.0
+// compare equal, as the contract wants, and pages outside the candidates enter as -inf (a
+// finite input never scores -inf; NaN scores are outside the contract).  With 16-byte rows
+// the scores reach shared memory by TMA tile loads, one warp's 32 rows x 16 pages per tile
+// (topk_tma_kernel); other layouts are read by per-thread loads (topk_thread_kernel).
 //
 // Larger top_k (the warp kernels below): one warp per row.
 // Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
@@ -46,21 +48,23 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The float a key was made from (+0.0 for the key of either zero).
-__device__ __forceinline__ float key_score(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
-}
-
-__device__ __forceinline__ void cmpx_desc(uint32_t& a, uint32_t& b) {  // a <- max, b <- min
-  const uint32_t hi = max(a, b);
-  b = min(a, b);
+__device__ __forceinline__ void cmpx_desc(float& a, float& b) {  // a <- max, b <- min
+  const float hi = fmaxf(a, b);
+  b = fminf(a, b);
   a = hi;
 }
 
-// Sorts 16 keys in descending order: Batcher's odd-even merge sort (K. E. Batcher, "Sorting
+// The least float above t (t finite; either zero gives the least positive subnormal).
+__device__ __forceinline__ float next_up(float t) {
+  const uint32_t u = __float_as_uint(t);
+  if ((u & 0x7fffffffu) == 0u) return __uint_as_float(1u);
+  return __uint_as_float(t > 0.f ? u + 1u : u - 1u);
+}
+
+// Sorts 16 scores in descending order: Batcher's odd-even merge sort (K. E. Batcher, "Sorting
 // networks and their applications", AFIPS 1968), 63 comparators in its ten layers, written
 // out so that every index is a constant.
-__device__ __forceinline__ void sort16_desc(uint32_t (&x)[16]) {
+__device__ __forceinline__ void sort16_desc(float (&x)[16]) {
 #define C(a, b) cmpx_desc(x[a], x[b])
   C(0, 1); C(2, 3); C(4, 5); C(6, 7); C(8, 9); C(10, 11); C(12, 13); C(14, 15);
   C(0, 2); C(1, 3); C(4, 6); C(5, 7); C(8, 10); C(9, 11); C(12, 14); C(13, 15);
@@ -76,9 +80,9 @@ __device__ __forceinline__ void sort16_desc(uint32_t (&x)[16]) {
 }
 
 // best <- the 16 largest of best and g (both descending), descending.
-__device__ __forceinline__ void merge16_desc(uint32_t (&best)[16], const uint32_t (&g)[16]) {
+__device__ __forceinline__ void merge16_desc(float (&best)[16], const float (&g)[16]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) best[i] = max(best[i], g[15 - i]);
+  for (int i = 0; i < 16; ++i) best[i] = fmaxf(best[i], g[15 - i]);
 #pragma unroll
   for (int s = 8; s >= 1; s >>= 1)
 #pragma unroll
@@ -108,27 +112,27 @@ __device__ __forceinline__ void load_group(const float* row, int base, int o, fl
     f[q] = base + 4 * q < o ? load4_raw<VEC>(row, base + 4 * q, o) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Pass 1 of a row: the keys of pages base .. base+15 that lie below o join the running list
+// Pass 1 of a row: the scores of pages base .. base+15 that lie below o join the running list
 // of the 16 largest.
-__device__ __forceinline__ void take_group(uint32_t (&best)[16], const float4 (&f)[4], int base,
+__device__ __forceinline__ void take_group(float (&best)[16], const float4 (&f)[4], int base,
                                            int o) {
-  uint32_t g[16];
+  float g[16];
   if (base + 16 <= o) {  // a full group: every page is a candidate
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      g[4 * q + 0] = score_key(f[q].x);
-      g[4 * q + 1] = score_key(f[q].y);
-      g[4 * q + 2] = score_key(f[q].z);
-      g[4 * q + 3] = score_key(f[q].w);
+      g[4 * q + 0] = f[q].x;
+      g[4 * q + 1] = f[q].y;
+      g[4 * q + 2] = f[q].z;
+      g[4 * q + 3] = f[q].w;
     }
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int c = base + 4 * q;
-      g[4 * q + 0] = c + 0 < o ? score_key(f[q].x) : 0u;
-      g[4 * q + 1] = c + 1 < o ? score_key(f[q].y) : 0u;
-      g[4 * q + 2] = c + 2 < o ? score_key(f[q].z) : 0u;
-      g[4 * q + 3] = c + 3 < o ? score_key(f[q].w) : 0u;
+      g[4 * q + 0] = c + 0 < o ? f[q].x : -INFINITY;
+      g[4 * q + 1] = c + 1 < o ? f[q].y : -INFINITY;
+      g[4 * q + 2] = c + 2 < o ? f[q].z : -INFINITY;
+      g[4 * q + 3] = c + 3 < o ? f[q].w : -INFINITY;
     }
   }
   sort16_desc(g);
@@ -136,33 +140,32 @@ __device__ __forceinline__ void take_group(uint32_t (&best)[16], const float4 (&
 }
 
 // The selection rule read off the list (o >= K >= 2 candidates, so the (K-1)-th and K-th
-// largest keys both exist), t being the (K-1)-th largest key.  When the K-th key differs from t,
-// the chosen candidates are exactly those with score >= t's score.  When it equals t (shared),
-// every candidate above t is taken and `need` of those equal to it, the lowest pages first.
+// largest scores both exist), t being the (K-1)-th largest.  When the K-th differs from t, the
+// chosen candidates are exactly those with score >= t.  When it equals t (shared), every
+// candidate above t is taken and `need` of those equal to it, the lowest pages first.
 struct TopkRule {
   float ge;  // while need == 0 the pages with score >= ge are taken
-  float eq;  // t's score: with need > 0, pages above it and `need` more equal to it are taken
+  float eq;  // t: with need > 0, the pages above it and `need` more equal to it are taken
   int need;
 };
 
-__device__ __forceinline__ TopkRule selection_rule(const uint32_t (&best)[16], int K) {
+__device__ __forceinline__ TopkRule selection_rule(const float (&best)[16], int K) {
   // the list is descending: t = best[K-2] is the least of the first K-1 entries, t_next =
   // best[K-1] the largest of the rest (reductions, so that no entry is picked by a run-time index)
-  uint32_t t = 0xffffffffu, t_next = 0u;
+  float t = INFINITY, t_next = -INFINITY;
   int above = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    t = i < K - 1 ? min(t, best[i]) : t;
-    t_next = i >= K - 1 ? max(t_next, best[i]) : t_next;
+    t = i < K - 1 ? fminf(t, best[i]) : t;
+    t_next = i >= K - 1 ? fmaxf(t_next, best[i]) : t_next;
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) above += best[i] > t ? 1 : 0;
   TopkRule rule;
   const bool shared = t_next == t;
-  rule.eq = key_score(t);
-  // shared: once the equal pages are in, the threshold is the least score above t's (the key
-  // order is the score order, so that is the score of key t + 1)
-  rule.ge = shared ? key_score(t + 1u) : rule.eq;
+  rule.eq = t;
+  // shared: once the equal pages are in, the threshold is the least score above t's
+  rule.ge = shared ? next_up(t) : t;
   rule.need = shared ? K - 1 - above : 0;
   return rule;
 }
@@ -252,9 +255,9 @@ topk_thread_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
       stage_short_row(so, o, K);
     } else {
       const float* row = scores + r * pitch;
-      uint32_t best[16];
+      float best[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) best[i] = 0u;
+      for (int i = 0; i < 16; ++i) best[i] = -INFINITY;
       float4 f[4];
       load_group<VEC>(row, 0, o, f);
       for (int base = 0; base < o; base += 16) {
@@ -283,8 +286,9 @@ topk_thread_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
 // tile load (64-byte swizzle: the 16-byte chunk c of tile row t sits at chunk c ^ ((t >> 1) & 3),
 // so the 32 threads' reads of their own rows hit distinct banks).  Each warp runs its own ring
 // of S tiles: its pass 1 over groups 0 .. G-1 and its pass 2 over them again are one sequence
-// of 2G tile loads, issued S ahead by lane 0.  G is the largest group count of the warp's rows.  Waits are bounded; a warp that gives up raises DEV_TIMEOUT and leaves
-// its rows unwritten.
+// of 2G tile loads, issued S ahead by lane 0.  G is the largest group count of the warp's
+// rows.  Waits are bounded; a warp that gives up raises DEV_TIMEOUT and leaves its rows
+// unwritten.
 constexpr int kTopkTile = 32 * 16 * 4;  // bytes of one tile
 template <int S>
 constexpr size_t topk_smem() {
@@ -352,9 +356,9 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
   if (lane == 0)
     for (int n = 0; n < S && n < items; ++n)
       topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
-  uint32_t best[16];
+  float best[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) best[i] = 0u;
+  for (int i = 0; i < 16; ++i) best[i] = -INFINITY;
   TopkRule rule{};
   bool ok = true;
   int pos = 0;
