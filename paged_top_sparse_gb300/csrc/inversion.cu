@@ -23,8 +23,10 @@
 //
 // When every chunk's block fits on the GPU at once (the usual case), one cooperative launch
 // runs all four steps (fused_kernel): the masks stay in shared memory and the selections in
-// registers from step 1 to step 4, two bounded grid barriers separate the steps, and every
-// block does step 3 itself.  Otherwise three kernels run: count, scan (a block per bucket for
+// registers from step 1 to step 4, and bounded grid barriers separate the steps: with few
+// buckets two (every block then does step 3 for all buckets itself), with many three (each
+// block scans the buckets of its own range in step 2 and sums them, a barrier, each block
+// offsets its range from the range sums, a barrier).  Otherwise three kernels run: count, scan (a block per bucket for
 // step 2; the last block to finish, found by an atomic ticket after a memory fence with no
 // waiting, does step 3) and emit (which rebuilds the masks).
 #include "ptx.cuh"
@@ -351,6 +353,45 @@ emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
   }
 }
 
+// Step 2 for one bucket, by the whole block: its chunk counts (written by other blocks, so read
+// past L1) become bucket-local exclusive offsets, and its total goes to bucket_totals.
+__device__ __forceinline__ void scan_bucket_block(const DevPlan& p, int bk, int* sh) {
+  const int gp = bk / p.Hkv, gg = bk % p.Hkv;
+  const ReqInfo& rb = p.reqs[p.page_req[gp]];
+  int32_t* cnt = p.chunk_offsets + chunk_id(p, rb, gp - rb.page_base, gg, 0);
+  const int n = rb.ch_per_bucket;
+  const int per = (n + 255) / 256;
+  const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+  int x = 0;
+  for (int i = i0; i < i1; ++i) x += __ldcg(cnt + i);
+  int off;
+  const int total = block_exclusive_scan(x, &off, sh);
+  for (int i = i0; i < i1; ++i) {
+    const int v = __ldcg(cnt + i);
+    cnt[i] = off;
+    off += v;
+  }
+  if (threadIdx.x == 0) p.bucket_totals[bk] = total;
+}
+
+// The same by one warp, for a bucket of at most 32 chunks (lane i holds chunk i).
+__device__ __forceinline__ void scan_bucket_warp(const DevPlan& p, int bk, int lane) {
+  const int gp = bk / p.Hkv, gg = bk % p.Hkv;
+  const ReqInfo& rb = p.reqs[p.page_req[gp]];
+  int32_t* cnt = p.chunk_offsets + chunk_id(p, rb, gp - rb.page_base, gg, 0);
+  const int n = rb.ch_per_bucket;
+  const int x = lane < n ? __ldcg(cnt + lane) : 0;
+  int incl = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane < n) cnt[lane] = incl - x;
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (lane == 0) p.bucket_totals[bk] = total;
+}
+
 // All the steps in one cooperative launch, one block per chunk (as count_kernel): the page
 // masks of every window stay in shared memory and the row's selections in registers from
 // the count to the emit, and two grid barriers replace the kernel boundaries.  After the
@@ -402,36 +443,35 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
     }
   }
   if (!grid_barrier(bar, p.status, &flag)) return;
-  // ---- 2. chunk offsets within each bucket, bucket totals
-  for (int bk = blockIdx.x; bk < p.num_buckets; bk += gridDim.x) {
-    const int gp = bk / p.Hkv, gg = bk % p.Hkv;
-    const ReqInfo& rb = p.reqs[p.page_req[gp]];
-    int32_t* cnt = p.chunk_offsets + chunk_id(p, rb, gp - rb.page_base, gg, 0);
-    const int n = rb.ch_per_bucket;
-    const int per = (n + 255) / 256;
-    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
-    int x = 0;
-    for (int i = i0; i < i1; ++i) x += __ldcg(cnt + i);
-    int off;
-    const int total = block_exclusive_scan(x, &off, sh);
-    for (int i = i0; i < i1; ++i) {
-      const int v = __ldcg(cnt + i);
-      cnt[i] = off;
-      off += v;
-    }
-    if (threadIdx.x == 0) p.bucket_totals[bk] = total;
+  // ---- 2. chunk offsets within each bucket, bucket totals.  Few buckets: a block per bucket,
+  // then a grid barrier.  Many: each block takes the buckets of its own range of step 3 (a
+  // warp per bucket of at most 32 chunks, the whole block for larger ones), so that its range
+  // sums (3a) follow without a grid barrier between them.
+  const int nb = p.num_buckets;
+  const bool few = nb <= 2 * (int)blockDim.x;
+  const int G = gridDim.x;
+  const int rper = (nb + G - 1) / G;  // buckets of each block's range (many buckets)
+  const int r0 = few ? 0 : min(nb, blockIdx.x * rper), r1 = few ? 0 : min(nb, r0 + rper);
+  if (few) {
+    for (int bk = blockIdx.x; bk < nb; bk += G) scan_bucket_block(p, bk, sh);
+    if (!grid_barrier(bar, p.status, &flag)) return;
+  } else {
+    for (int bk = r0 + warp; bk < r1; bk += blockDim.x / 32)
+      if (p.reqs[p.page_req[bk / p.Hkv]].ch_per_bucket <= 32) scan_bucket_warp(p, bk, lane);
+    for (int bk = r0; bk < r1; ++bk)  // the same condition for every thread of the block
+      if (p.reqs[p.page_req[bk / p.Hkv]].ch_per_bucket > 32) scan_bucket_block(p, bk, sh);
+    __syncthreads();  // the range's totals are written
   }
-  if (!grid_barrier(bar, p.status, &flag)) return;
   // ---- 3. exclusive scans over the bucket totals (entries and work items), which give every
   // bucket's CSR offset and its work items.  Few buckets: every block scans them all and keeps
   // the offsets of its own buckets (its request and KV head, every page) for the emit.  Many
-  // buckets (more than two per thread): each block sums its own range of buckets, a third grid
-  // barrier, then each block scans the ranges' sums (one per block), writes its range's
-  // offsets and work items, and after a fourth barrier reads its own buckets' offsets.
+  // buckets (more than two per thread): each block sums its own range of buckets (the ones it
+  // scanned in step 2), a grid barrier, then each block scans the ranges' sums (one per block),
+  // writes its range's offsets and work items, and after another barrier reads its own
+  // buckets' offsets.
   __shared__ int s_boff[kMaxPagesPerReq];  // CSR offset of page pg's bucket of this block's KV head
-  const int nb = p.num_buckets;
   const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
-  if (nb <= 2 * (int)blockDim.x) {
+  if (few) {
     const int per = (nb + 255) / 256;
     const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
     int cnt = 0, ntask = 0;
@@ -471,9 +511,6 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
       if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
     }
   } else {
-    const int G = gridDim.x;
-    const int rper = (nb + G - 1) / G;  // buckets of each block's range
-    const int r0 = min(nb, blockIdx.x * rper), r1 = min(nb, r0 + rper);
     // 3a. this block's range: its sums of entries and of work items
     {
       int cnt = 0, ntask = 0;
