@@ -195,6 +195,7 @@ def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     ([100], [9000], 2),
     ([120], [5000], 1),
     ([64], [40000], 16),                   # 313 pages: twenty groups of 16
+    ([5], [2100], 16),                     # 20 rows (< 32: per-thread loads), 17 pages
 ])
 def test_topk_strided_scores(q_lens, ctx_lens, k, pad):
     """The score buffer as a view whose row pitch exceeds max_pages (pad 0 and 4: a pitch that
