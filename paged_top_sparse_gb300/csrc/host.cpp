@@ -182,10 +182,12 @@ sps_status validate_problem(const sps_problem* p) {
   int64_t R = T * p->num_q_heads;
   if (R * p->top_k >= ((int64_t)1 << 31) || R * p->head_dim >= ((int64_t)1 << 40))
     return fail(SPS_EUNSUPPORTED, "batch too large (rows x top_k must stay below 2^31)");
-  if (p->max_pages_per_req > kMaxPagesPerReq)
+  const int page_cap = p->top_k <= 16 ? kMaxPagesPerReq : kMaxPagesWideK;
+  if (p->max_pages_per_req > page_cap)
     return fail(SPS_EUNSUPPORTED,
-                "max_pages_per_req above %d (%dK tokens of context per request) is not supported",
-                kMaxPagesPerReq, kMaxPagesPerReq * kPage / 1024);
+                "max_pages_per_req above %d (%dK tokens of context per request) is not supported "
+                "with top_k %d",
+                page_cap, page_cap * kPage / 1024, p->top_k);
   return SPS_OK;
 }
 

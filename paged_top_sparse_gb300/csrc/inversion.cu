@@ -469,7 +469,7 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
   // scanned in step 2), a grid barrier, then each block scans the ranges' sums (one per block),
   // writes its range's offsets and work items, and after another barrier reads its own
   // buckets' offsets.
-  __shared__ int s_boff[kMaxPagesPerReq];  // CSR offset of page pg's bucket of this block's KV head
+  __shared__ int s_boff[kInvFusedMaxPages];  // CSR offset of page pg's bucket of this block's KV head
   const int own0 = ri ? ri->page_base * p.Hkv + g : -1;  // this block's bucket of page 0
   if (few) {
     const int per = (nb + 255) / 256;
@@ -618,7 +618,9 @@ fused_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
 template <int KV>
 bool try_fused(const DevPlan& p, const int32_t* idx, float* lse, int64_t lse_split_stride,
                cudaStream_t st, cudaError_t* err) {
-  // max_pages bounds every request's page count, so it sizes the 64-page windows
+  // max_pages bounds every request's page count, so it sizes the 64-page windows and must fit
+  // the per-block offset table
+  if (p.max_pages > kInvFusedMaxPages) return false;
   const int nwin = (p.max_pages + kInvPages - 1) / kInvPages;
   const size_t dsmem = (size_t)2 * nwin * kInvPages * (kChunkWords + 1) * sizeof(uint32_t);
   auto kern = fused_kernel<KV>;

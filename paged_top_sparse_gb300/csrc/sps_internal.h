@@ -12,8 +12,13 @@ constexpr int kMaxTopK = 64;
 constexpr int kFwdTaskGroups = 8;  // 128-row query groups per forward work item
 constexpr int kChunkWords = 8;     // 32-row words per inversion chunk (one 256-thread block)
 constexpr int kInvPages = 64;      // pages per inversion window (one 64-bit row mask)
-constexpr int kMaxPagesPerReq = 1024;  // visible pages of one request (128K tokens): the top-k
-                                       // lane layouts and the inversion's offset table
+// Visible pages of one request: 8192 (1M tokens) with top_k <= 16, where the inversion packs a
+// page into 16 bits; 1024 (128K tokens) with top_k > 16, whose warp-per-row top-k holds at most
+// 32 pages per lane.  The single-launch inversion keeps a 1024-entry offset table per block, so
+// longer requests take its three-kernel form.
+constexpr int kMaxPagesPerReq = 8192;
+constexpr int kMaxPagesWideK = 1024;
+constexpr int kInvFusedMaxPages = 1024;
 
 // One request of the batch, as the kernels see it.
 struct ReqInfo {

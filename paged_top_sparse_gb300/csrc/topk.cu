@@ -691,7 +691,7 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
   } else if (p.max_pages <= 768) {
     e = launch_pdl(topk_filter_kernel<24, 32>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   } else {
-    static_assert(kMaxPagesPerReq <= 32 * 32, "the widest lane layouts hold 32 x 32 pages");
+    static_assert(kMaxPagesWideK <= 32 * 32, "the widest lane layouts hold 32 x 32 pages");
     e = launch_pdl(topk_filter_kernel<32, 32>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
   }
   return e != cudaSuccess ? e : cudaGetLastError();

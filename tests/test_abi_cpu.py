@@ -89,12 +89,23 @@ def test_combine_validation_needs_no_device(L):
     assert b"split_stride" in L.sps_last_error()
 
 
-def test_plan_rejects_more_than_1024_pages_per_request(L):
-    """The top-k lane layouts and the inversion's offset table are sized for at most 1024
-    visible pages (128K tokens of context per request); a plan beyond that is refused with a
-    message naming the limit."""
-    _plan(q_lens=[200], ctx_lens=[130800], max_pages_per_req=1024, num_phys_pages=1024)
+def test_plan_page_limits(L):
+    """With top_k <= 16 a request may see up to 8192 pages (1M tokens of context: the
+    inversion packs a page into 16 bits); with top_k > 16 up to 1024 (128K tokens: the
+    warp-per-row top-k holds at most 32 pages per lane).  A plan beyond its limit is refused
+    with a message naming it."""
+    _plan(q_lens=[16], ctx_lens=[1048560], max_pages_per_req=8192, num_phys_pages=8192,
+          num_q_heads=2, num_kv_heads=1, head_dim=64)
     with pytest.raises(B.SpsError) as e:
-        _plan(q_lens=[200], ctx_lens=[130900], max_pages_per_req=1025, num_phys_pages=1025)
+        _plan(q_lens=[16], ctx_lens=[1048570], max_pages_per_req=8193, num_phys_pages=8193,
+              num_q_heads=2, num_kv_heads=1, head_dim=64)
     assert e.value.status == 2
-    assert "1024" in str(e.value)
+    assert "8192" in str(e.value)
+    _plan(q_lens=[200], ctx_lens=[130800], max_pages_per_req=1024, num_phys_pages=1024, top_k=17)
+    with pytest.raises(B.SpsError) as e:
+        _plan(q_lens=[200], ctx_lens=[130900], max_pages_per_req=1025, num_phys_pages=1025,
+              top_k=17)
+    assert e.value.status == 2
+    assert "1024" in str(e.value) and "top_k 17" in str(e.value)
+    # a 1025-page request with top_k <= 16 is a valid plan
+    _plan(q_lens=[200], ctx_lens=[130900], max_pages_per_req=1025, num_phys_pages=1025)

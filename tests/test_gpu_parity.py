@@ -57,9 +57,13 @@ def _workload(name):
     if name == "maxctx":  # 512 pages, 64K tokens
         return synth.workload("custom", seed=41, q_lens=[200], ctx_lens=[65300], num_q_heads=4,
                               num_kv_heads=2, head_dim=128, top_k=16)
-    if name == "ctx128k":  # the largest page count a plan takes (1024 pages, 128K tokens)
+    if name == "ctx128k":  # 1024 pages, 128K tokens: the single-launch inversion's widest case
         return synth.workload("custom", seed=43, q_lens=[200], ctx_lens=[130800],
                               num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=16)
+    if name == "ctx1m":  # 8192 pages, 1M tokens: the largest page count a plan takes (top_k 16);
+        # 32 rows, so top-k runs its TMA form; the inversion runs its three-kernel form
+        return synth.workload("custom", seed=44, q_lens=[16], ctx_lens=[1048560],
+                              num_q_heads=2, num_kv_heads=1, head_dim=64, top_k=16)
     if name == "with_empty":  # requests without new tokens between others
         return synth.workload("custom", seed=42, q_lens=[0, 150, 0, 33],
                               ctx_lens=[500, 700, 0, 1000], num_q_heads=4, num_kv_heads=2,
@@ -72,7 +76,7 @@ def _workload(name):
 
 
 SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64",
-         "maxctx", "ctx128k", "with_empty"]
+         "maxctx", "ctx128k", "ctx1m", "with_empty"]
 FULL = ["prefill8k", "prefill8k_q", "chunked32k"]
 _cache = {}
 
