@@ -79,7 +79,9 @@ enum {
  *   head_dim           D: 64 or 128
  *   page_size          must be 128
  *   top_k              k: 1..64 pages kept per row
- *   max_pages_per_req  row length of the page table, >= every request's visible page count
+ *   max_pages_per_req  row length of the page table, >= every request's visible page count;
+ *                      at most 8192 (1M tokens) with top_k <= 16 and 1024 (128K tokens) with
+ *                      larger top_k, else SPS_EUNSUPPORTED
  *   num_phys_pages     number of physical pages in the K/V caches
  *   q_dtype / kv_dtype           attention inputs: BF16/BF16 or E4M3/NVFP4
  *   idx_q_dtype / idx_k_dtype    indexer inputs: BF16/BF16, E4M3/E4M3 or E4M3/NVFP4
