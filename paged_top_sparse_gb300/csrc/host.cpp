@@ -308,7 +308,10 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   int64_t upload_end = off;
   pl->off_chunk_offsets = take(4 * (pl->num_chunks + 1));
   pl->off_bucket_totals = take(4 * pl->num_buckets);
-  pl->off_range_sums = take(8 * std::max<int64_t>(1, pl->inv_blocks));
+  // per block of the single-launch inversion, or of the multi-kernel one's scan: its range's
+  // entries and work items
+  pl->off_range_sums = take(8 * std::max<int64_t>(
+      {int64_t(1), pl->inv_blocks, (pl->num_buckets + kInvScanBuckets - 1) / kInvScanBuckets}));
   pl->off_bucket_offsets = take(4 * (pl->num_buckets + 1));
   pl->off_entries = take(8 * std::max<int64_t>(1, pl->max_entries));
   pl->off_fwd_tasks = take(sizeof(FwdTask) * pl->max_fwd_tasks);
@@ -511,8 +514,8 @@ sps_status fwd_common(const sps_plan* pl, const void* q, float q_scale, const vo
     return fail(SPS_EUNSUPPORTED, "sparse_prefill_fwd_fp8qk: needs E4M3 Q, NVFP4 K/V, D = 128");
   DevPlan d = make_dev_plan(pl, ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // no counter needs clearing here: the inversion writes the task count, and its scan ticket
-  // and grid barrier return to zero when they complete (the plan upload clears them first)
+  // no counter needs clearing here: the inversion writes the task count, and its grid barrier
+  // returns to zero when it completes (the plan upload clears it first)
   cudaError_t e = launch_inversion(d, idx, lse, lse_split_stride, s);
   if (e != cudaSuccess) return cuda_fail(e, "inversion launch");
   if (kind == FwdKind::kFP8QK)

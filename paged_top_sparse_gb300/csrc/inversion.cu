@@ -26,9 +26,12 @@
 // registers from step 1 to step 4, and bounded grid barriers separate the steps: with few
 // buckets two (every block then does step 3 for all buckets itself), with many three (each
 // block scans the buckets of its own range in step 2 and sums them, a barrier, each block
-// offsets its range from the range sums, a barrier).  Otherwise three kernels run: count, scan (a block per bucket for
-// step 2; the last block to finish, found by an atomic ticket after a memory fence with no
-// waiting, does step 3) and emit (which rebuilds the masks).
+// offsets its range from the range sums, a barrier).  Otherwise (or when a request sees more
+// than 1024 pages) four kernels run: count and emit (which rebuilds the masks) with a block per
+// chunk and group of eight 64-page windows, so that a long request's windows are spread over
+// the grid; between them the scan (step 2, a block per eight buckets, which also sums each
+// block's range) and the offsets (step 3 on the same grid: each block offsets its buckets by
+// the range sums before it).
 #include "ptx.cuh"
 #include "sps_internal.h"
 
@@ -204,20 +207,28 @@ __device__ __forceinline__ void build_masks(uint32_t (*tm)[kInvPages][kChunkWord
   __syncthreads();
 }
 
+// Windows of one block of the three-kernel form (blockIdx.y picks the group of the chunk's
+// request's windows), so that a long request's windows are spread over the grid.
+constexpr int kInvGroupWins = 8;
+
 template <int KV>
-__global__ void __launch_bounds__(256, 8)
+__global__ void __launch_bounds__(256, 4)
 count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse,
              int64_t lse_split_stride) {
-  __shared__ uint32_t tm[1][kInvPages][kChunkWords + 1];
+  __shared__ uint32_t tm[kInvGroupWins][kInvPages][kChunkWords + 1];
   int g, c;
   const int b = find_block(p, blockIdx.x, &g, &c);
   if (b < 0) return;  // uniform over the block
   const ReqInfo& ri = p.reqs[b];
+  const int nwin = (ri.npages + kInvPages - 1) / kInvPages;
+  const int w0 = (int)blockIdx.y * kInvGroupWins;
+  if (w0 >= nwin) return;  // uniform
+  const int w1 = min(nwin, w0 + kInvGroupWins);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
   RowSel<KV> sel;
   sel.load(idx, rc, p.K);
-  if (rc.valid) {
+  if (rc.valid && blockIdx.y == 0) {
 #pragma unroll
     for (int s = 0; s < sel.n(); ++s) {
       if (s >= p.K) break;
@@ -226,130 +237,187 @@ count_kernel(DevPlan p, const int32_t* __restrict__ idx, float* __restrict__ lse
       else if (pg > rc.o) set_status(p.status, DEV_BAD_INDEX);
     }
   }
-  for (int wi = 0; wi * kInvPages < ri.npages; ++wi) {
-    build_masks(tm, wi, wi + 1, sel, rc, warp, lane);
-    const int d = threadIdx.x, p0 = wi * kInvPages;
-    if (d < kInvPages && p0 + d < ri.npages) {
+  build_masks(tm, w0, w1, sel, rc, warp, lane);
+  for (int i = threadIdx.x; i < (w1 - w0) * kInvPages; i += blockDim.x) {
+    const int wi = i / kInvPages, d = i % kInvPages, pg = (w0 + wi) * kInvPages + d;
+    if (pg < ri.npages) {
       int n = 0;
 #pragma unroll 8
-      for (int v = 0; v < kChunkWords; ++v) n += __popc(tm[0][d][v]);
-      p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)] = n;  // a count until step 2
+      for (int v = 0; v < kChunkWords; ++v) n += __popc(tm[wi][d][v]);
+      p.chunk_offsets[chunk_id(p, ri, pg, g, c)] = n;  // a count until step 2
     }
-    __syncthreads();
   }
 }
 
-// Step 3 (one block): bucket totals -> CSR offsets (in place), then the forward's work list.
-// The totals were written by other blocks of this grid, so they are read past L1.
-__device__ __forceinline__ void scan_buckets(const DevPlan& p, int* sh) {
-  const int nb = p.num_buckets, nt = blockDim.x;
-  const int per = (nb + nt - 1) / nt;
-  const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
-  const int per_task = kFwdTaskGroups * 128;
-  int cnt = 0, ntask = 0;
-  for (int b = b0; b < b1; ++b) {
-    const int t = __ldcg(p.bucket_offsets + b);
-    cnt += t;
-    ntask += (t + per_task - 1) / per_task;
-  }
-  int off, toff;
-  const int total = block_exclusive_scan(cnt, &off, sh);
-  const int ttotal = block_exclusive_scan(ntask, &toff, sh);
-  for (int b = b0; b < b1; ++b) {
-    const int t = __ldcg(p.bucket_offsets + b);
-    p.bucket_offsets[b] = off;
-    for (int e = off; e < off + t; e += per_task) {
-      if (toff < p.max_fwd_tasks) {
-        FwdTask ft;
-        ft.bucket = b;
-        ft.entry_begin = e;
-        ft.count = min(per_task, off + t - e);
-        ft.pad = 0;
-        p.fwd_tasks[toff] = ft;
-      }
-      ++toff;
-    }
-    off += t;
-  }
-  if (threadIdx.x == 0) {
-    p.bucket_offsets[nb] = total;
-    if (total > p.max_entries) set_status(p.status, DEV_OVERFLOW);
-    p.counters[2] = min(ttotal, p.max_fwd_tasks);
-    if (ttotal > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
-  }
-}
+// Step 2: a block per eight buckets turns their chunk counts into bucket-local exclusive
+// offsets (a warp per bucket of at most 32 chunks, the block for larger ones) and leaves each
+// bucket's total in bucket_offsets[bucket]; the last block to finish runs step 3.
+constexpr int kScanBuckets = kInvScanBuckets;
 
-// Step 2: a block per bucket turns its chunk counts into bucket-local exclusive offsets and
-// leaves the bucket's total in bucket_offsets[bucket]; the last block to finish runs step 3.
 __global__ void __launch_bounds__(256) scan_kernel(DevPlan p) {
   __shared__ int sh[32];
-  __shared__ int last;
-  const int bk = blockIdx.x;
-  const int gp = bk / p.Hkv, g = bk % p.Hkv;
-  const ReqInfo ri = p.reqs[p.page_req[gp]];
-  int32_t* cnt = p.chunk_offsets + chunk_id(p, ri, gp - ri.page_base, g, 0);
-  const int n = ri.ch_per_bucket;
-  const int per = (n + 255) / 256;
-  const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
-  int x = 0;
-  for (int i = i0; i < i1; ++i) x += cnt[i];
-  int off;
-  const int total = block_exclusive_scan(x, &off, sh);
-  for (int i = i0; i < i1; ++i) {
-    const int v = cnt[i];
-    cnt[i] = off;
-    off += v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bk0 = (int)blockIdx.x * kScanBuckets;
+  // a bucket of at most 32 chunks: one warp, lane i holding chunk i
+  if (bk0 + warp < p.num_buckets) {
+    const int bk = bk0 + warp, gp = bk / p.Hkv, g = bk % p.Hkv;
+    const ReqInfo& ri = p.reqs[p.page_req[gp]];
+    const int n = ri.ch_per_bucket;
+    if (n <= 32) {
+      int32_t* cnt = p.chunk_offsets + chunk_id(p, ri, gp - ri.page_base, g, 0);
+      const int x = lane < n ? cnt[lane] : 0;
+      int incl = x;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      if (lane < n) cnt[lane] = incl - x;
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) p.bucket_offsets[bk] = total;
+    }
   }
-  if (threadIdx.x == 0) p.bucket_offsets[bk] = total;
-  __threadfence();  // this block's results are visible before its ticket
+  // larger buckets: the whole block, one after another (the same test for every thread)
+  for (int j = 0; j < kScanBuckets && bk0 + j < p.num_buckets; ++j) {
+    const int bk = bk0 + j, gp = bk / p.Hkv, g = bk % p.Hkv;
+    const ReqInfo& ri = p.reqs[p.page_req[gp]];
+    const int n = ri.ch_per_bucket;
+    if (n <= 32) continue;
+    int32_t* cnt = p.chunk_offsets + chunk_id(p, ri, gp - ri.page_base, g, 0);
+    const int per = (n + 255) / 256;
+    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+    int x = 0;
+    for (int i = i0; i < i1; ++i) x += cnt[i];
+    int off;
+    const int total = block_exclusive_scan(x, &off, sh);
+    for (int i = i0; i < i1; ++i) {
+      const int v = cnt[i];
+      cnt[i] = off;
+      off += v;
+    }
+    if (threadIdx.x == 0) p.bucket_offsets[bk] = total;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(p.counters + 3, 1) == p.num_buckets - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // every block has taken its ticket: the counter goes back to zero for the next call
-  if (threadIdx.x == 0) p.counters[3] = 0;
-  scan_buckets(p, sh);
+  // this block's range: its buckets' entries and work items
+  if (warp == 0) {
+    const int bk = bk0 + lane;
+    const int per_task = kFwdTaskGroups * 128;
+    const int t = lane < kScanBuckets && bk < p.num_buckets ? p.bucket_offsets[bk] : 0;
+    int c = t, n = (t + per_task - 1) / per_task;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      c += __shfl_xor_sync(0xffffffffu, c, d);
+      n += __shfl_xor_sync(0xffffffffu, n, d);
+    }
+    if (lane == 0) {
+      p.range_sums[blockIdx.x] = c;
+      p.range_sums[gridDim.x + blockIdx.x] = n;
+    }
+  }
+}
+
+// Step 3 of the multi-kernel form, on the scan's grid: each block offsets its buckets by the
+// range sums of the blocks before it and writes their CSR offsets and work items; block 0 also
+// the total.
+__global__ void __launch_bounds__(256) offsets_kernel(DevPlan p) {
+  __shared__ int sh[32];
+  const int G = gridDim.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cnt = 0, ntask = 0, tot = 0, ttot = 0;
+  for (int b = threadIdx.x; b < G; b += blockDim.x) {
+    const int c = p.range_sums[b], t = p.range_sums[G + b];
+    tot += c;
+    ttot += t;
+    if (b < (int)blockIdx.x) {
+      cnt += c;
+      ntask += t;
+    }
+  }
+  int unused;
+  cnt = block_exclusive_scan(cnt, &unused, sh);
+  ntask = block_exclusive_scan(ntask, &unused, sh);
+  tot = block_exclusive_scan(tot, &unused, sh);
+  ttot = block_exclusive_scan(ttot, &unused, sh);
+  if (warp != 0) return;
+  const int per_task = kFwdTaskGroups * 128;
+  const int bk = (int)blockIdx.x * kScanBuckets + lane;
+  const bool mine = lane < kScanBuckets && bk < p.num_buckets;
+  const int t = mine ? p.bucket_offsets[bk] : 0;
+  const int nt = (t + per_task - 1) / per_task;
+  int o = t, to = nt;  // inclusive scans over the block's buckets
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, o, d), z = __shfl_up_sync(0xffffffffu, to, d);
+    if (lane >= d) {
+      o += y;
+      to += z;
+    }
+  }
+  o += cnt - t;
+  to += ntask - nt;
+  if (mine) {
+    p.bucket_offsets[bk] = o;
+    for (int j = 0; j < nt; ++j) {
+      if (to + j < p.max_fwd_tasks) {
+        FwdTask ft;
+        ft.bucket = bk;
+        ft.entry_begin = o + j * per_task;
+        ft.count = min(per_task, t - j * per_task);
+        ft.pad = 0;
+        p.fwd_tasks[to + j] = ft;
+      }
+    }
+  }
+  if (blockIdx.x == 0 && lane == 0) {
+    p.bucket_offsets[p.num_buckets] = tot;
+    if (tot > p.max_entries) set_status(p.status, DEV_OVERFLOW);
+    p.counters[2] = min(ttot, p.max_fwd_tasks);
+    if (ttot > p.max_fwd_tasks) set_status(p.status, DEV_OVERFLOW);
+  }
 }
 
 template <int KV>
-__global__ void __launch_bounds__(256, 8)
+__global__ void __launch_bounds__(256, 4)
 emit_kernel(DevPlan p, const int32_t* __restrict__ idx) {
-  __shared__ uint32_t tm[1][kInvPages][kChunkWords + 1];
-  __shared__ int pos0[kInvPages][kChunkWords + 1];  // first entry of (page, warp)
+  __shared__ uint32_t tm[kInvGroupWins][kInvPages][kChunkWords + 1];
+  __shared__ int pos0[kInvGroupWins][kInvPages][kChunkWords + 1];  // first entry of (page, warp)
   pdl_trigger();  // the forward that follows may start its prologue
   int g, c;
   const int b = find_block(p, blockIdx.x, &g, &c);
   if (b < 0) return;  // uniform over the block
   const ReqInfo& ri = p.reqs[b];
+  const int nwin = (ri.npages + kInvPages - 1) / kInvPages;
+  const int w0 = (int)blockIdx.y * kInvGroupWins;
+  if (w0 >= nwin) return;  // uniform
+  const int w1 = min(nwin, w0 + kInvGroupWins);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowCtx rc = row_of(p, ri, g, c * kChunkWords + warp, lane);
   RowSel<KV> sel;
   sel.load(idx, rc, p.K);
   const uint32_t below = (1u << lane) - 1u;
-  for (int p0 = 0; p0 < ri.npages; p0 += kInvPages) {
-    build_masks(tm, p0 / kInvPages, p0 / kInvPages + 1, sel, rc, warp, lane);
-    const int d = threadIdx.x;
-    if (d < kInvPages && p0 + d < ri.npages) {
-      const int bk = (ri.page_base + p0 + d) * p.Hkv + g;
-      int acc = p.bucket_offsets[bk] + p.chunk_offsets[chunk_id(p, ri, p0 + d, g, c)];
+  build_masks(tm, w0, w1, sel, rc, warp, lane);
+  for (int i = threadIdx.x; i < (w1 - w0) * kInvPages; i += blockDim.x) {
+    const int wi = i / kInvPages, d = i % kInvPages, pg = (w0 + wi) * kInvPages + d;
+    if (pg < ri.npages) {
+      const int bk = (ri.page_base + pg) * p.Hkv + g;
+      int acc = p.bucket_offsets[bk] + p.chunk_offsets[chunk_id(p, ri, pg, g, c)];
       for (int v = 0; v < kChunkWords; ++v) {
-        pos0[d][v] = acc;
-        acc += __popc(tm[0][d][v]);
+        pos0[wi][d][v] = acc;
+        acc += __popc(tm[wi][d][v]);
       }
     }
-    __syncthreads();
-    if (rc.valid) {
+  }
+  __syncthreads();
+  if (rc.valid) {
 #pragma unroll
-      for (int s = 0; s < sel.n(); ++s) {
-        const int pg = sel.get(s);
-        const int dd = pg - p0;
-        if (dd < 0 || dd >= kInvPages || pg > rc.o) continue;
-        const int pos = pos0[dd][warp] + __popc(tm[0][dd][warp] & below);
-        p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
-      }
+    for (int s = 0; s < sel.n(); ++s) {
+      const int pg = sel.get(s);
+      if (pg < 0 || pg > rc.o) continue;
+      const int w = pg / kInvPages;
+      if (w < w0 || w >= w1) continue;
+      const int wi = w - w0, d = pg % kInvPages;
+      const int pos = pos0[wi][d][warp] + __popc(tm[wi][d][warp] & below);
+      p.entries[pos] = make_int2((int)rc.r, (rc.t << 6) | s);
     }
-    __syncthreads();
   }
 }
 
@@ -654,19 +722,23 @@ cudaError_t launch_inversion(const DevPlan& p, const int32_t* idx, float* lse,
   if (kv == 16 ? try_fused<16>(p, idx, lse, lse_split_stride, st, &e)
                : try_fused<0>(p, idx, lse, lse_split_stride, st, &e))
     return e;
+  // a block per (chunk, group of kInvGroupWins windows of the chunk's request)
+  const dim3 grid((unsigned)p.inv_blocks,
+                  (unsigned)((p.max_pages + kInvPages * kInvGroupWins - 1) / (kInvPages * kInvGroupWins)));
   const unsigned nblk = (unsigned)p.inv_blocks;
   if (nblk > 0) {
-    if (kv == 16) count_kernel<16><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);
-    else count_kernel<0><<<nblk, 256, 0, st>>>(p, idx, lse, lse_split_stride);
+    if (kv == 16) count_kernel<16><<<grid, 256, 0, st>>>(p, idx, lse, lse_split_stride);
+    else count_kernel<0><<<grid, 256, 0, st>>>(p, idx, lse, lse_split_stride);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // counters[3] (buckets scanned) is zero: the plan upload clears it and each scan's last block
-  // puts it back to zero
-  scan_kernel<<<(unsigned)p.num_buckets, 256, 0, st>>>(p);
+  const unsigned nscan = (unsigned)((p.num_buckets + kScanBuckets - 1) / kScanBuckets);
+  scan_kernel<<<nscan, 256, 0, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  offsets_kernel<<<nscan, 256, 0, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nblk > 0) {
-    if (kv == 16) emit_kernel<16><<<nblk, 256, 0, st>>>(p, idx);
-    else emit_kernel<0><<<nblk, 256, 0, st>>>(p, idx);
+    if (kv == 16) emit_kernel<16><<<grid, 256, 0, st>>>(p, idx);
+    else emit_kernel<0><<<grid, 256, 0, st>>>(p, idx);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

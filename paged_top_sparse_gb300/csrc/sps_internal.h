@@ -19,6 +19,7 @@ constexpr int kInvPages = 64;      // pages per inversion window (one 64-bit row
 constexpr int kMaxPagesPerReq = 8192;
 constexpr int kMaxPagesWideK = 1024;
 constexpr int kInvFusedMaxPages = 1024;
+constexpr int kInvScanBuckets = 8;  // buckets per block of the multi-kernel inversion's scan
 
 // One request of the batch, as the kernels see it.
 struct ReqInfo {
@@ -54,10 +55,9 @@ struct DevPlan {
   int32_t inv_blocks;       // sum over requests of H_kv * ch_per_bucket
   float sm_scale;
   int32_t* status;
-  int32_t* counters;        // [2] fwd task count, [3] inversion buckets scanned, [4] [5]
-                            // inversion grid barrier (arrivals, generation); [0] [1] unused.
-                            // Zeroed by the plan upload; [3] and [4] return to zero when
-                            // their scan / barrier completes
+  int32_t* counters;        // [2] fwd task count, [4] [5] inversion grid barrier (arrivals,
+                            // generation); [0] [1] [3] unused.  Zeroed by the plan upload;
+                            // [4] returns to zero when the barrier completes
   const int32_t* tok_pos;   // [T]
   const int32_t* tok_req;   // [T]
   const ReqInfo* reqs;      // [batch]
