@@ -336,7 +336,7 @@ def _e2e_pipelined(args, flush, stream, in_pairs, step, copy_out, nbuf=2):
 
 def _launches_per_step(w, fp8qk, inv_launches):
     """Kernels of this library one step launches: plan upload, indexer, top-k, the inversion
-    (one cooperative launch, or three kernels), forward, combine, plus the quantised paths'
+    (one cooperative launch, or four kernels), forward, combine, plus the quantised paths'
     copies (the indexer's FP16 Q and visible key pages over NVFP4 keys; the forward's FP16 Q
     on the exact route)."""
     n = 5 + inv_launches
@@ -455,10 +455,11 @@ def run_prefill(args, world, dev, wname, partials="fp32", fp8qk=False, data=None
     k_ms = per.mean(0)
     names = ["indexer", "topk", "fwd", "combine"]
     # the inversion is one cooperative launch when its 256-row blocks fit on the GPU at once
-    # (8 per SM), else three kernels
+    # (8 per SM) and no request sees more than 1024 pages, else four kernels
     hg = w.num_q_heads // w.num_kv_heads
     inv_blocks = sum(w.num_kv_heads * -(-(-(-ql * hg // 32)) // 8) for ql in w.q_lens)
-    inv_launches = 1 if inv_blocks <= 8 * torch.cuda.get_device_properties(dev).multi_processor_count else 3
+    fits = inv_blocks <= 8 * torch.cuda.get_device_properties(dev).multi_processor_count
+    inv_launches = 1 if fits and w.max_pages <= 1024 else 4
     kern = {
         "indexer": {"us": k_ms[0] * 1e3, "achieved": alg["indexer_flops"] / (k_ms[0] * 1e-3) / 1e12,
                     "unit": "TFLOP/s", "peak": idx_peak, "bound": "tensor",
