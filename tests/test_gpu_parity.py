@@ -61,7 +61,7 @@ def _workload(name):
         return synth.workload("custom", seed=43, q_lens=[200], ctx_lens=[130800],
                               num_q_heads=4, num_kv_heads=2, head_dim=128, top_k=16)
     if name == "ctx1m":  # 8192 pages, 1M tokens: the largest page count a plan takes (top_k 16);
-        # 32 rows, so top-k runs its TMA form; the inversion runs its three-kernel form
+        # 32 rows, so top-k runs its TMA form; the inversion runs its multi-kernel form
         return synth.workload("custom", seed=44, q_lens=[16], ctx_lens=[1048560],
                               num_q_heads=2, num_kv_heads=1, head_dim=64, top_k=16)
     if name == "with_empty":  # requests without new tokens between others
@@ -645,7 +645,7 @@ def test_grid_barrier_times_out_without_hanging():
 
 def test_inversion_when_the_single_launch_does_not_fit():
     """12000 tokens x 16 heads per KV group: 1500 inversion chunks, more blocks than the GPU
-    holds at once, so the inversion takes its three-kernel path; the CSR offsets and entries
+    holds at once, so the inversion takes its multi-kernel path; the CSR offsets and entries
     must still match the oracle bit for bit (and the 8K workloads above cover the
     single-launch path)."""
     from tests.gpu_helpers import DeviceRun
@@ -671,7 +671,7 @@ def test_repeated_forward_after_one_upload(q_len):
     """Three forward calls on one uploaded workspace give bit-identical partials, LSEs and
     outputs: the inversion's scan ticket and grid barrier return to zero after each call, so no
     call clears counters.  300 tokens take the single cooperative inversion launch, 12000 tokens
-    x 32 heads the three-kernel path."""
+    x 32 heads the multi-kernel path."""
     from tests.gpu_helpers import DeviceRun
 
     w = synth.workload("custom", seed=32, q_lens=[q_len], ctx_lens=[200], num_q_heads=32,
