@@ -134,7 +134,10 @@ struct sps_plan {
           off_page_req = 0, off_idx_tasks = 0, off_chunk_offsets = 0, off_bucket_totals = 0,
           off_range_sums = 0,
           off_qconv = -1, off_kconv = -1,
-          off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, ws_bytes = 0;
+          off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, off_topk_lists = -1,
+          ws_bytes = 0;
+  int64_t fwd_ws_bytes = 0;  // the part the forward uses (the no-allocation forward's need)
+  int32_t topk_nseg = 1, topk_segg = 0;
   int64_t upload_bytes = 0;  // [0, upload_bytes) of the workspace comes from `blob`
   std::vector<uint8_t> blob;
 };
@@ -326,6 +329,21 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   if (idx_fp16)
     pl->off_kconv = take(2 * std::max<int64_t>(1, pl->total_pages) * p.num_kv_heads * kPage *
                          p.head_dim);
+  pl->fwd_ws_bytes = off;
+  // Top-k with top_k <= 16 runs a thread per row, so long rows of a small batch leave few
+  // warps, each walking hundreds of 16-page groups one after another.  From 64 groups on, pass
+  // 1 is split into segments of at least 32 groups, enough of them for ~24 warps per SM of a
+  // 152-SM GPU; each segment's 16 largest scores go to this area and merge per row.
+  const int64_t groups = (p.max_pages_per_req + 15) / 16;
+  if (p.top_k > 1 && p.top_k <= 16 && groups >= 64) {
+    const int64_t warps = (pl->R + 31) / 32, target = 24 * 152;
+    const int64_t nseg = std::min<int64_t>(groups / 32, (target + warps - 1) / warps);
+    if (nseg >= 2) {
+      pl->topk_nseg = (int32_t)nseg;
+      pl->topk_segg = (int32_t)((groups + nseg - 1) / nseg);
+      pl->off_topk_lists = take(4 * 16 * pl->R * nseg);
+    }
+  }
   pl->ws_bytes = off;
 
   // the host image of [0, upload_end): the status word and counters (zero), then the metadata
@@ -405,6 +423,10 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.fwd_tasks = reinterpret_cast<FwdTask*>(base + pl->off_fwd_tasks);
   d.qconv = pl->off_qconv >= 0 ? base + pl->off_qconv : nullptr;
   d.kconv = pl->off_kconv >= 0 ? base + pl->off_kconv : nullptr;
+  d.topk_lists = pl->off_topk_lists >= 0 ? reinterpret_cast<float*>(base + pl->off_topk_lists)
+                                         : nullptr;
+  d.topk_nseg = pl->topk_nseg;
+  d.topk_segg = pl->topk_segg;
   return d;
 }
 
@@ -855,11 +877,11 @@ sps_status sps_internal_fwd_noalloc(const sps_plan* pl, const void* q, float q_s
   if (lse_split_stride < pl->R) return fail(SPS_EINVAL, "lse_split_stride must be >= rows");
   if (!std::isfinite(q_scale)) return fail(SPS_EINVAL, "q_scale must be finite");
   if (dev_status && !aligned(dev_status, 4)) return fail(SPS_EINVAL, "dev_status misaligned");
-  if ((int64_t)scratch_bytes < pl->ws_bytes)
+  if ((int64_t)scratch_bytes < pl->fwd_ws_bytes)
     return fail(SPS_ENOSPACE,
                 "sparse_prefill_fwd_noalloc: this batch needs %lld bytes of scratch, the built-in "
                 "array holds %zu; split the batch or use sparse_prefill_fwd with a workspace",
-                (long long)pl->ws_bytes, scratch_bytes);
+                (long long)pl->fwd_ws_bytes, scratch_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(scratch);
   // the array keeps the previous call's contents: one copy zeroes the status word and

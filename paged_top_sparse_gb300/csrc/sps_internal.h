@@ -77,6 +77,11 @@ struct DevPlan {
   // page_base + logical page)
   void* qconv;
   void* kconv;
+  // top_k <= 16 over long rows: pass 1 of each row split into topk_nseg segments of topk_segg
+  // 16-page groups, each segment's 16 largest scores in topk_lists [rows][topk_nseg][16]
+  // (topk_nseg 1: no split, topk_lists null)
+  float* topk_lists;
+  int32_t topk_nseg, topk_segg;
 };
 
 // Launch of `kern` that may overlap the previous kernel in the stream (programmatic stream

@@ -295,14 +295,21 @@ constexpr size_t topk_smem() {
   return 1024 + 8 * S * kTopkTile + 8 * S * 8 + 256 * kTopkOP * 4;
 }
 
-// Lane 0 of a warp: the tile load of item n of its sequence (group n, or n - G in pass 2)
-// into stage n % S.
+// Lane 0 of a warp: the tile load of item n of its sequence, 16-page group `group`, into
+// stage n % S.
+template <int S>
+__device__ __forceinline__ void topk_issue_group(const CUtensorMap* tm, uint32_t tiles,
+                                                 uint32_t bars, int n, int group, int r0) {
+  const int s = n % S;
+  mbar_expect_tx(bars + 8 * s, kTopkTile);
+  tma_load_2d(tiles + s * kTopkTile, tm, 16 * group, r0, bars + 8 * s);
+}
+
+// The same for a sequence of pass 1 over groups 0 .. G-1, then pass 2 over them again.
 template <int S>
 __device__ __forceinline__ void topk_issue_tile(const CUtensorMap* tm, uint32_t tiles,
                                                 uint32_t bars, int n, int G, int r0) {
-  const int s = n % S;
-  mbar_expect_tx(bars + 8 * s, kTopkTile);
-  tma_load_2d(tiles + s * kTopkTile, tm, 16 * (n < G ? n : n - G), r0, bars + 8 * s);
+  topk_issue_group<S>(tm, tiles, bars, n, n < G ? n : n - G, r0);
 }
 
 // Every lane waits for item n's tile (stage n % S); true on all lanes when it landed.
@@ -320,7 +327,81 @@ __device__ __forceinline__ void topk_read_tile(const uint8_t* tile, int lane, fl
   for (int c = 0; c < 4; ++c) f[c] = *reinterpret_cast<const float4*>(row + 16 * (c ^ sw));
 }
 
+// Pass 1 of long rows split into segments (DevPlan::topk_nseg): warp w of block (x, y) runs
+// pass 1 of its 32 rows over the 16-page groups [y * segg, (y + 1) * segg), through the same
+// per-warp tile ring, and stores each full row's 16 largest scores of the segment (descending)
+// to topk_lists[row][y]; a segment past a row's last candidate stores nothing.
 template <int S>
+__global__ void __launch_bounds__(256)
+topk_seg_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + 8 * S * kTopkTile);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t my_tiles = smem_u32(tiles + warp * S * kTopkTile);
+  const uint32_t my_bars = smem_u32(bars + warp * S);
+  if (lane == 0) {
+    tma_prefetch_desc(&tmS);
+    for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_wait();  // the scores come from the indexer just before
+  const int64_t R = (int64_t)p.T * p.H;
+  const int64_t r0 = (int64_t)blockIdx.x * 256 + warp * 32;
+  if (r0 >= R) return;  // warp-uniform; this warp issued no copy
+  const int64_t r = r0 + lane;
+  const int K = p.K;
+  int o = 0;
+  bool full = false;
+  if (r < R) {
+    o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
+    full = o >= K && K > 1;
+  }
+  const int Gw = (int)__reduce_max_sync(0xffffffffu, full ? (uint32_t)(o + 15) / 16u : 0u);
+  const int g0 = (int)blockIdx.y * p.topk_segg;
+  const int g1 = min(Gw, g0 + p.topk_segg);
+  const int items = g1 > g0 ? g1 - g0 : 0;
+  if (lane == 0)  // item n of this warp's sequence is group g0 + n
+    for (int n = 0; n < S && n < items; ++n)
+      topk_issue_group<S>(&tmS, my_tiles, my_bars, n, g0 + n, (int)r0);
+  float best[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) best[i] = -INFINITY;
+  bool ok = true;
+  for (int n = 0; n < items; ++n) {
+    const int s = n % S;
+    if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
+      ok = false;
+      break;
+    }
+    const int base = 16 * (g0 + n);
+    if (full && base < o) {
+      float4 f[4];
+      topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
+      take_group(best, f, base, o);
+    }
+    __syncwarp();
+    if (lane == 0 && n + S < items)
+      topk_issue_group<S>(&tmS, my_tiles, my_bars, n + S, g0 + n + S, (int)r0);
+  }
+  if (!ok) {  // let the copies already issued land before the block's shared memory is reused
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
+    return;
+  }
+  if (full && 16 * g0 < o) {
+    float4* dst = reinterpret_cast<float4*>(p.topk_lists + (r * p.topk_nseg + blockIdx.y) * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_float4(best[4 * q], best[4 * q + 1], best[4 * q + 2], best[4 * q + 3]);
+  }
+}
+
+// SEG: pass 1 comes from topk_seg_kernel's per-segment lists, merged here; the tile sequence
+// is pass 2 alone.
+template <int S, bool SEG>
 __global__ void __launch_bounds__(256)
 topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
   extern __shared__ uint8_t smem_raw[];
@@ -352,7 +433,8 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
     if (!full) stage_short_row(so, o, K);
   }
   const int G = (int)__reduce_max_sync(0xffffffffu, full ? (uint32_t)(o + 15) / 16u : 0u);
-  const int items = 2 * G;
+  const int p2 = SEG ? 0 : G;  // first item of pass 2
+  const int items = p2 + G;
   if (lane == 0)
     for (int n = 0; n < S && n < items; ++n)
       topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
@@ -362,9 +444,25 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
   TopkRule rule{};
   bool ok = true;
   int pos = 0;
+  if (SEG && full) {  // pass 1 from the segments' lists (descending), merged
+    for (int sg = 0; sg < p.topk_nseg && 16 * sg * p.topk_segg < o; ++sg) {
+      const float4* src =
+          reinterpret_cast<const float4*>(p.topk_lists + (r * p.topk_nseg + sg) * 16);
+      float g[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = __ldg(src + q);
+        g[4 * q] = v.x;
+        g[4 * q + 1] = v.y;
+        g[4 * q + 2] = v.z;
+        g[4 * q + 3] = v.w;
+      }
+      merge16_desc(best, g);
+    }
+  }
   // pass 1: groups 0 .. G-1 into the running list
   int n = 0;
-  for (; n < G; ++n) {
+  for (; n < p2; ++n) {
     const int s = n % S;
     if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
       ok = false;
@@ -387,10 +485,10 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
       ok = false;
       break;
     }
-    if (full && 16 * (n - G) < o) {
+    if (full && 16 * (n - p2) < o) {
       float4 f[4];
       topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
-      emit_group(f, 16 * (n - G), o, rule, so, pos);
+      emit_group(f, 16 * (n - p2), o, rule, so, pos);
     }
     __syncwarp();
     if (lane == 0 && n + S < items)
@@ -643,11 +741,26 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
 template <int S>
 cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, int32_t* idx, unsigned grid,
                             cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(topk_tma_kernel<S>,
+  if (p.topk_nseg > 1 && p.topk_lists) {  // long rows: pass 1 by segments, then the merge
+    cudaError_t e = cudaFuncSetAttribute(topk_seg_kernel<S>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)topk_smem<S>());
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_seg_kernel<S>, dim3(grid, (unsigned)p.topk_nseg), dim3(256),
+                   topk_smem<S>(), st, tm, p);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_tma_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topk_smem<S>());
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_tma_kernel<S, true>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p,
+                      idx);
+  }
+  cudaError_t e = cudaFuncSetAttribute(topk_tma_kernel<S, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)topk_smem<S>());
   if (e != cudaSuccess) return e;
-  return launch_pdl(topk_tma_kernel<S>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p, idx);
+  return launch_pdl(topk_tma_kernel<S, false>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p,
+                    idx);
 }
 
 cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, int32_t* idx,

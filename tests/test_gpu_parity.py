@@ -165,6 +165,9 @@ def test_topk_bit_exact_on_shared_scores(name):
     ([40], [89000], 16),          # 696 pages
     ([30], [127900], 16),         # 1000 pages
     ([20], [130900], 64),         # 1023 pages, the largest k
+    ([20], [200000], 16),         # 1563 pages: pass 1 in segments merged per row
+    ([12], [500000], 5),          # 3907 pages, segments
+    ([8], [1048000], 16),         # 8192 pages (the limit), sixteen segments
 ])
 def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     """Scores drawn from {-1.5, ..., 1.5} with signed zeros: most pages tie with others, so
@@ -200,6 +203,7 @@ def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     ([120], [5000], 1),
     ([64], [40000], 16),                   # 313 pages: twenty groups of 16
     ([5], [2100], 16),                     # 20 rows (< 32: per-thread loads), 17 pages
+    ([40], [300000], 16),                  # 2345 pages: pass 1 in segments (16-byte pitch)
 ])
 def test_topk_strided_scores(q_lens, ctx_lens, k, pad):
     """The score buffer as a view whose row pitch exceeds max_pages (pad 0 and 4: a pitch that
