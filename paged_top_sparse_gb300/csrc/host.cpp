@@ -135,6 +135,7 @@ struct sps_plan {
           off_range_sums = 0,
           off_qconv = -1, off_kconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, off_topk_lists = -1,
+          off_topk_meta = -1,
           ws_bytes = 0;
   int64_t fwd_ws_bytes = 0;  // the part the forward uses (the no-allocation forward's need)
   int32_t topk_nseg = 1, topk_segg = 0;
@@ -342,6 +343,7 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
       pl->topk_nseg = (int32_t)nseg;
       pl->topk_segg = (int32_t)((groups + nseg - 1) / nseg);
       pl->off_topk_lists = take(4 * 16 * pl->R * nseg);
+      pl->off_topk_meta = take(4 * (2 + nseg) * pl->R);
     }
   }
   pl->ws_bytes = off;
@@ -425,6 +427,8 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.kconv = pl->off_kconv >= 0 ? base + pl->off_kconv : nullptr;
   d.topk_lists = pl->off_topk_lists >= 0 ? reinterpret_cast<float*>(base + pl->off_topk_lists)
                                          : nullptr;
+  d.topk_meta = pl->off_topk_meta >= 0 ? reinterpret_cast<int32_t*>(base + pl->off_topk_meta)
+                                       : nullptr;
   d.topk_nseg = pl->topk_nseg;
   d.topk_segg = pl->topk_segg;
   return d;

@@ -80,7 +80,10 @@ struct DevPlan {
   // top_k <= 16 over long rows: pass 1 of each row split into topk_nseg segments of topk_segg
   // 16-page groups, each segment's 16 largest scores in topk_lists [rows][topk_nseg][16]
   // (topk_nseg 1: no split, topk_lists null)
+  // and, per row, [0] 1 when pass 2 runs by segments, [1] the threshold, [2 + s] where segment
+  // s's pages start in the row's output: topk_meta [rows][2 + topk_nseg]
   float* topk_lists;
+  int32_t* topk_meta;
   int32_t topk_nseg, topk_segg;
 };
 

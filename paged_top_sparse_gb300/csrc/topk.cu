@@ -327,6 +327,19 @@ __device__ __forceinline__ void topk_read_tile(const uint8_t* tile, int lane, fl
   for (int c = 0; c < 4; ++c) f[c] = *reinterpret_cast<const float4*>(row + 16 * (c ^ sw));
 }
 
+// A segment's stored list: 16 floats, descending.
+__device__ __forceinline__ void load_list(const float* src, float (&g)[16]) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = __ldg(s4 + q);
+    g[4 * q] = v.x;
+    g[4 * q + 1] = v.y;
+    g[4 * q + 2] = v.z;
+    g[4 * q + 3] = v.w;
+  }
+}
+
 // Pass 1 of long rows split into segments (DevPlan::topk_nseg): warp w of block (x, y) runs
 // pass 1 of its 32 rows over the 16-page groups [y * segg, (y + 1) * segg), through the same
 // per-warp tile ring, and stores each full row's 16 largest scores of the segment (descending)
@@ -399,8 +412,88 @@ topk_seg_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p) {
   }
 }
 
+// Pass 2 of long rows by segments, after topk_tma_kernel<S, true> left it to this kernel
+// (topk_meta[row][0] = 1): warp w of block (x, y) walks its rows' groups of segment y and
+// writes the pages at or above the row's threshold, in order, from the segment's start in the
+// row's output on.  The own page (slot k-1) and every other row were written by that kernel.
+template <int S>
+__global__ void __launch_bounds__(256)
+topk_emit_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + 8 * S * kTopkTile);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t my_tiles = smem_u32(tiles + warp * S * kTopkTile);
+  const uint32_t my_bars = smem_u32(bars + warp * S);
+  if (lane == 0) {
+    tma_prefetch_desc(&tmS);
+    for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_wait();  // the row kernel's thresholds and offsets
+  const int64_t R = (int64_t)p.T * p.H;
+  const int64_t r0 = (int64_t)blockIdx.x * 256 + warp * 32;
+  if (r0 >= R) return;  // warp-uniform; this warp issued no copy
+  const int64_t r = r0 + lane;
+  const int K = p.K, nseg = p.topk_nseg;
+  const int g0 = (int)blockIdx.y * p.topk_segg;
+  int o = 0, off = 0;
+  float ge = 0.f;
+  bool act = false;
+  if (r < R) {
+    o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
+    if (o >= K && K > 1 && 16 * g0 < o) {
+      const int32_t* meta = p.topk_meta + r * (2 + nseg);
+      act = meta[0] == 1;
+      ge = __int_as_float(meta[1]);
+      off = meta[2 + blockIdx.y];
+    }
+  }
+  const int Gw = (int)__reduce_max_sync(0xffffffffu, act ? (uint32_t)(o + 15) / 16u : 0u);
+  const int g1 = min(Gw, g0 + p.topk_segg);
+  const int items = g1 > g0 ? g1 - g0 : 0;
+  if (lane == 0)
+    for (int n = 0; n < S && n < items; ++n)
+      topk_issue_group<S>(&tmS, my_tiles, my_bars, n, g0 + n, (int)r0);
+  int32_t* out = idx + r * K;
+  bool ok = true;
+  for (int n = 0; n < items; ++n) {
+    const int s = n % S;
+    if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
+      ok = false;
+      break;
+    }
+    const int base = 16 * (g0 + n);
+    if (act && base < o) {
+      float4 f[4];
+      topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
+      const float v[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
+                           f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
+      uint32_t bits = 0u;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) bits |= v[e] >= ge ? 1u << e : 0u;
+      if (o - base < 16) bits &= (1u << (o - base)) - 1u;
+      while (bits) {
+        if (off < K - 1) out[off] = base + __ffs(bits) - 1;  // in bounds whatever the scores
+        ++off;
+        bits &= bits - 1u;
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && n + S < items)
+      topk_issue_group<S>(&tmS, my_tiles, my_bars, n + S, g0 + n + S, (int)r0);
+  }
+  if (!ok) {  // let the copies already issued land before the block's shared memory is reused
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
+  }
+}
+
 // SEG: pass 1 comes from topk_seg_kernel's per-segment lists, merged here; the tile sequence
-// is pass 2 alone.
+// is pass 2 alone, and only for warps with a row whose threshold is shared (the others leave
+// pass 2 to topk_emit_kernel).
 template <int S, bool SEG>
 __global__ void __launch_bounds__(256)
 topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
@@ -433,33 +526,52 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
     if (!full) stage_short_row(so, o, K);
   }
   const int G = (int)__reduce_max_sync(0xffffffffu, full ? (uint32_t)(o + 15) / 16u : 0u);
-  const int p2 = SEG ? 0 : G;  // first item of pass 2
-  const int items = p2 + G;
-  if (lane == 0)
-    for (int n = 0; n < S && n < items; ++n)
-      topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
   float best[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) best[i] = -INFINITY;
   TopkRule rule{};
   bool ok = true;
   int pos = 0;
-  if (SEG && full) {  // pass 1 from the segments' lists (descending), merged
-    for (int sg = 0; sg < p.topk_nseg && 16 * sg * p.topk_segg < o; ++sg) {
-      const float4* src =
-          reinterpret_cast<const float4*>(p.topk_lists + (r * p.topk_nseg + sg) * 16);
-      float g[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = __ldg(src + q);
-        g[4 * q] = v.x;
-        g[4 * q + 1] = v.y;
-        g[4 * q + 2] = v.z;
-        g[4 * q + 3] = v.w;
+  bool walk = true;  // SEG: this warp runs pass 2 itself
+  if (SEG) {
+    // pass 1 from the segments' lists (descending), merged; then, unless some row of the warp
+    // shares its threshold, every full row leaves pass 2 to topk_emit_kernel: its threshold
+    // and, per segment, where the segment's pages start in the row's output (the count of
+    // earlier lists' entries at or above the threshold: with the threshold not shared, exactly
+    // k - 1 candidates reach it, and each lies in its segment's list)
+    const int nseg = p.topk_nseg;
+    if (full) {
+      for (int sg = 0; sg < nseg && 16 * sg * p.topk_segg < o; ++sg) {
+        float g[16];
+        load_list(p.topk_lists + (r * nseg + sg) * 16, g);
+        merge16_desc(best, g);
       }
-      merge16_desc(best, g);
+      rule = selection_rule(best, K);
+    }
+    walk = __any_sync(0xffffffffu, full && rule.need > 0);
+    if (full) {
+      int32_t* meta = p.topk_meta + r * (2 + nseg);
+      meta[0] = walk ? 0 : 1;
+      meta[1] = __float_as_int(rule.ge);
+      if (!walk) {
+        int acc = 0;
+        for (int sg = 0; sg < nseg; ++sg) {
+          meta[2 + sg] = acc;
+          if (16 * sg * p.topk_segg < o) {
+            float g[16];
+            load_list(p.topk_lists + (r * nseg + sg) * 16, g);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc += g[i] >= rule.ge ? 1 : 0;
+          }
+        }
+      }
     }
   }
+  const int p2 = SEG ? 0 : G;  // first item of pass 2
+  const int items = SEG && !walk ? 0 : p2 + G;
+  if (lane == 0)
+    for (int n = 0; n < S && n < items; ++n)
+      topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
   // pass 1: groups 0 .. G-1 into the running list
   int n = 0;
   for (; n < p2; ++n) {
@@ -477,7 +589,7 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
     if (lane == 0 && n + S < items)
       topk_issue_tile<S>(&tmS, my_tiles, my_bars, n + S, G, (int)r0);
   }
-  if (full) rule = selection_rule(best, K);
+  if (!SEG && full) rule = selection_rule(best, K);
   // pass 2: the same groups again, the chosen pages in ascending order
   for (; ok && n < items; ++n) {
     const int s = n % S;
@@ -752,8 +864,14 @@ cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, int32_t* id
     e = cudaFuncSetAttribute(topk_tma_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)topk_smem<S>());
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_tma_kernel<S, true>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p,
-                      idx);
+    e = launch_pdl(topk_tma_kernel<S, true>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p,
+                   idx);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_emit_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)topk_smem<S>());
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_emit_kernel<S>, dim3(grid, (unsigned)p.topk_nseg), dim3(256),
+                      topk_smem<S>(), st, tm, p, idx);
   }
   cudaError_t e = cudaFuncSetAttribute(topk_tma_kernel<S, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

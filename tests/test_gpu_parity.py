@@ -195,6 +195,41 @@ def test_topk_ties_and_signed_zeros(q_lens, ctx_lens, k):
     assert np.array_equal(idx.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("k", [16, 9, 2])
+def test_topk_long_rows_by_segments(k):
+    """Rows of ~4700 pages in a batch of 128 rows: pass 1 runs in segments, and pass 2 by
+    segments for the warps whose rows all have an unshared threshold (warps 1 and 3, N(0,1)
+    scores) and row by row for the others (warps 0 and 2, scores from {-1, ..., 1} with signed
+    zeros, so thresholds are shared)."""
+    from paged_top_sparse_gb300 import binding as B
+
+    w = synth.workload("custom", seed=23, q_lens=[32], ctx_lens=[600000], num_q_heads=4,
+                       num_kv_heads=2, head_dim=128, top_k=k)
+    plan = B.Plan(w.q_lens, w.ctx_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.top_k,
+                  w.max_pages, w.num_phys_pages)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda:0")
+    B.sps_plan_upload(plan, ws)
+    rng = np.random.default_rng(7)
+    R, P = w.num_rows, w.max_pages
+    assert R == 128
+    s = rng.standard_normal((R, P)).astype(np.float32)
+    for wp in (0, 2):
+        t = (rng.integers(-2, 3, size=(32, P)) * 0.5).astype(np.float32)
+        t[rng.random((32, P)) < 0.2] = -0.0
+        s[32 * wp:32 * wp + 32] = t
+    _, tok_pos = orc.token_meta(oracle_problem(w))
+    own = (tok_pos[np.arange(R) // w.num_q_heads] // 128)[:, None]
+    s[np.arange(P)[None, :] > own] = np.nan
+    idx = torch.full((R, k), -7, dtype=torch.int32, device="cuda:0")
+    B.topk_select(plan, torch.from_numpy(s).cuda(), idx, ws)
+    torch.cuda.synchronize()
+    assert B.sps_read_device_status(plan, ws) == 0
+    ref = orc.topk(oracle_problem(w), np.nan_to_num(s.astype(np.float64), nan=-np.inf))
+    got = idx.cpu().numpy()
+    bad = np.nonzero(~np.all(got == ref, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
+
+
 @pytest.mark.parametrize("pad", [0, 1, 4])
 @pytest.mark.parametrize("q_lens,ctx_lens,k", [
     ([150, 90, 301], [2100, 700, 0], 16),  # three requests: rows of a warp see different pages
