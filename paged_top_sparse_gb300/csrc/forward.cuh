@@ -249,6 +249,14 @@ forward_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         mbar_expect_tx(vf, TILE);
         for (int db = 0; db < DB; ++db)
           tma_load_2d(smem_u32(sm.v) + db * 16384, &tmV, db * 64, krow, vf);
+        // items of a group or less (the plan's fwd_prefetch): the next item's tiles into L2
+        // while this one runs
+        const int tn = ti + p.fwd_prefetch * (int)gridDim.x;
+        if (p.fwd_prefetch > 0 && tn < ntasks) {
+          const int tile_n = item_tile(p, page_table, p.fwd_tasks[tn]);
+          bulk_prefetch_l2(kc + (int64_t)tile_n * TQK, TQK);
+          bulk_prefetch_l2(vc + (int64_t)tile_n * TILE, TILE);
+        }
       } else {
         // codes and scales of K, then of V, one item ahead of the conversion
         if (!mbar_wait(smem_u32(&sm.kraw_empty), (kv_it & 1) ^ 1, abort_flag, status)) break;

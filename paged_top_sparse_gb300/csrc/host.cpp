@@ -139,6 +139,7 @@ struct sps_plan {
           ws_bytes = 0;
   int64_t fwd_ws_bytes = 0;  // the part the forward uses (the no-allocation forward's need)
   int32_t topk_nseg = 1, topk_segg = 0;
+  int32_t fwd_prefetch = 0;
   int64_t upload_bytes = 0;  // [0, upload_bytes) of the workspace comes from `blob`
   std::vector<uint8_t> blob;
 };
@@ -331,6 +332,8 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
     pl->off_kconv = take(2 * std::max<int64_t>(1, pl->total_pages) * p.num_kv_heads * kPage *
                          p.head_dim);
   pl->fwd_ws_bytes = off;
+  // at most 128 entries per bucket on average: most work items are a single group
+  pl->fwd_prefetch = pl->max_entries <= 128 * std::max<int64_t>(1, pl->num_buckets) ? 1 : 0;
   // Top-k with top_k <= 16 runs a thread per row, so long rows of a small batch leave few
   // warps, each walking hundreds of 16-page groups one after another.  From 64 groups on, pass
   // 1 is split into segments of at least 32 groups, enough of them for ~24 warps per SM of a
@@ -430,6 +433,7 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.topk_meta = pl->off_topk_meta >= 0 ? reinterpret_cast<int32_t*>(base + pl->off_topk_meta)
                                        : nullptr;
   d.topk_nseg = pl->topk_nseg;
+  d.fwd_prefetch = pl->fwd_prefetch;
   d.topk_segg = pl->topk_segg;
   return d;
 }

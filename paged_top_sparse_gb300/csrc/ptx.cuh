@@ -143,6 +143,10 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies
+// A hint: `bytes` (a multiple of 16) at `src` (16-byte aligned) into L2, no completion.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }

@@ -85,6 +85,10 @@ struct DevPlan {
   float* topk_lists;
   int32_t* topk_meta;
   int32_t topk_nseg, topk_segg;
+  // forward, BF16 K/V: when buckets hold few rows (an item of one group or less, so every group
+  // waits for its own K/V tiles), the K/V tiles of the item this many items ahead are
+  // prefetched into L2 (0: none; the plan sets 1)
+  int32_t fwd_prefetch;
 };
 
 // Launch of `kern` that may overlap the previous kernel in the stream (programmatic stream
