@@ -159,10 +159,14 @@ def _algorithmic(w, idx_np, partial_bytes=4):
     }
 
 
-WORKLOADS = ("prefill8k", "prefill8k_q", "chunked32k", "combine_stress", "kv_append")
+WORKLOADS = ("prefill8k", "prefill8k_q", "chunked32k", "combine_stress", "kv_append", "ctx1m")
 
 
 def _describe(w, name):
+    if name == "ctx1m":
+        return (f"long context: 512 new tokens after {int(w.ctx_lens[0])} cached (1M tokens, "
+                f"{w.max_pages} pages), 32 q / 2 kv heads, head_dim 128, page 128, top-16, BF16 "
+                "(permuted physical pages)")
     if name == "chunked32k":
         return (f"chunked prefill: {w.batch} requests x 512 new tokens over {min(w.ctx_lens)}.."
                 f"{max(w.ctx_lens)} cached, 32 q / 2 kv heads, head_dim 128, page 128, top-16, "
@@ -334,12 +338,23 @@ def _e2e_pipelined(args, flush, stream, in_pairs, step, copy_out, nbuf=2):
     return t0.elapsed_time(t1) / args.steps
 
 
+def _topk_launches(w):
+    """Top-k kernels of one call: three (segments' pass 1, the rows, segments' pass 2) when the
+    plan splits long rows (top_k <= 16, 64 or more 16-page groups, few enough rows that the
+    split pays: the plan's own rule), else one."""
+    groups = (w.max_pages + 15) // 16
+    if not (1 < w.top_k <= 16 and groups >= 64 and w.num_rows >= 32):
+        return 1
+    warps = (w.num_rows + 31) // 32
+    return 3 if min(groups // 32, -(-(24 * 152) // warps)) >= 2 else 1
+
+
 def _launches_per_step(w, fp8qk, inv_launches):
-    """Kernels of this library one step launches: plan upload, indexer, top-k, the inversion
-    (one cooperative launch, or four kernels), forward, combine, plus the quantised paths'
-    copies (the indexer's FP16 Q and visible key pages over NVFP4 keys; the forward's FP16 Q
-    on the exact route)."""
-    n = 5 + inv_launches
+    """Kernels of this library one step launches: plan upload, indexer, top-k (one, or three
+    over long rows), the inversion (one cooperative launch, or four kernels), forward,
+    combine, plus the quantised paths' copies (the indexer's FP16 Q and visible key pages over
+    NVFP4 keys; the forward's FP16 Q on the exact route)."""
+    n = 4 + _topk_launches(w) + inv_launches
     if w.idx_dtype != "e4m3" and w.kv_dtype == "nvfp4":
         n += 2
     if w.q_dtype == "e4m3" and not fp8qk:
@@ -815,7 +830,8 @@ def main():
                     help="prefill length (8192 = the benchmark workload; others for profiling)")
     ap.add_argument("--workload", default="prefill8k", choices=WORKLOADS,
                     help="prefill8k (default: the headline line), prefill8k_q (E4M3 Q, NVFP4 "
-                         "K/V), chunked32k (8 x 512 over 32K context), combine_stress")
+                         "K/V), chunked32k (8 x 512 over 32K context), combine_stress, ctx1m "
+                         "(512 new tokens at the end of a 1M-token context)")
     ap.add_argument("--fp8qk", action="store_true",
                     help="quantised workload only: the pages' Q8KV4 route (K rounded to E4M3, "
                          "FP8 Q K^T) through sparse_prefill_fwd_fp8qk")

@@ -156,6 +156,9 @@ def workload(name: str, seed: int = 0, **over) -> Workload:
         ctx = np.round(32768 * rng.uniform(0.75, 1.25, size=8)).astype(np.int64)
         q_lens = np.full(8, 512)
         H, Hkv, D, k, permute = 32, 2, 128, 16, True
+    elif name == "ctx1m":  # a 512-token chunk at the end of a 1M-token context (8192 pages)
+        q_lens, ctx = np.array([512]), np.array([1048576 - 512])
+        H, Hkv, D, k, permute = 32, 2, 128, 16, True
     elif name == "custom":
         q_lens, ctx = np.asarray(over.pop("q_lens")), np.asarray(over.pop("ctx_lens"))
         H, Hkv = over.pop("num_q_heads"), over.pop("num_kv_heads")
