@@ -682,14 +682,19 @@ def test_grid_barrier_times_out_without_hanging():
     assert torch.allclose(out.float(), part.mean(0), atol=2e-2)
 
 
-def test_inversion_when_the_single_launch_does_not_fit():
-    """12000 tokens x 16 heads per KV group: 1500 inversion chunks, more blocks than the GPU
-    holds at once, so the inversion takes its multi-kernel path; the CSR offsets and entries
-    must still match the oracle bit for bit (and the 8K workloads above cover the
-    single-launch path)."""
+@pytest.mark.parametrize("q_len,ctx,H", [
+    (12000, 0, 32),      # 94 pages: one group of two 64-page windows (shared-memory ORs)
+    (8100, 0, 64),       # 64 pages: a single window (ballots)
+    (12000, 60000, 32),  # 563 pages: a group of eight windows and a single ninth
+])
+def test_inversion_when_the_single_launch_does_not_fit(q_len, ctx, H):
+    """Over 1216 inversion chunks (e.g. 12000 tokens x 16 heads per KV group: 1500), more
+    blocks than the GPU holds at once, so the inversion takes its multi-kernel path; the CSR
+    offsets and entries must still match the oracle bit for bit (and the 8K workloads above
+    cover the single-launch path)."""
     from tests.gpu_helpers import DeviceRun
 
-    w = synth.workload("custom", seed=31, q_lens=[12000], ctx_lens=[0], num_q_heads=32,
+    w = synth.workload("custom", seed=31, q_lens=[q_len], ctx_lens=[ctx], num_q_heads=H,
                        num_kv_heads=2, head_dim=128, top_k=16)
     run = DeviceRun(w, synth.make_tensors(w))
     run.run_all()
@@ -708,7 +713,7 @@ def test_inversion_when_the_single_launch_does_not_fit():
 @pytest.mark.parametrize("q_len", [300, 12000])
 def test_repeated_forward_after_one_upload(q_len):
     """Three forward calls on one uploaded workspace give bit-identical partials, LSEs and
-    outputs: the inversion's scan ticket and grid barrier return to zero after each call, so no
+    outputs: the inversion's grid barrier returns to zero after each call, so no
     call clears counters.  300 tokens take the single cooperative inversion launch, 12000 tokens
     x 32 heads the multi-kernel path."""
     from tests.gpu_helpers import DeviceRun
