@@ -64,6 +64,11 @@ def _workload(name):
         # 32 rows, so top-k runs its TMA form; the inversion runs its multi-kernel form
         return synth.workload("custom", seed=44, q_lens=[16], ctx_lens=[1048560],
                               num_q_heads=2, num_kv_heads=1, head_dim=64, top_k=16)
+    if name == "ctx1m_q":  # the same limit with E4M3 Q and NVFP4 K/V (the indexer's key-page
+        # conversion over 8192 pages, the forward's loader dequant), top-8
+        return synth.workload("custom", seed=45, q_lens=[16], ctx_lens=[1048560],
+                              num_q_heads=2, num_kv_heads=1, head_dim=64, top_k=8,
+                              q_dtype="e4m3", kv_dtype="nvfp4")
     if name == "with_empty":  # requests without new tokens between others
         return synth.workload("custom", seed=42, q_lens=[0, 150, 0, 33],
                               ctx_lens=[500, 700, 0, 1000], num_q_heads=4, num_kv_heads=2,
@@ -76,7 +81,7 @@ def _workload(name):
 
 
 SMALL = ["tiny", "ragged", "mha_d64", "k1", "chunked_fp8_small", "quant_small", "quant_d64",
-         "maxctx", "ctx128k", "ctx1m", "with_empty"]
+         "maxctx", "ctx128k", "ctx1m", "ctx1m_q", "with_empty"]
 FULL = ["prefill8k", "prefill8k_q", "chunked32k"]
 _cache = {}
 
