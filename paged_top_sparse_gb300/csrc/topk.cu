@@ -20,7 +20,11 @@
 // compare equal, as the contract wants, and pages outside the candidates enter as -inf (a
 // finite input never scores -inf; NaN scores are outside the contract).  With 16-byte rows
 // the scores reach shared memory by TMA tile loads, one warp's 32 rows x 16 pages per tile
-// (topk_tma_kernel); other layouts are read by per-thread loads (topk_thread_kernel).
+// (topk_tma_kernel); other layouts are read by per-thread loads (topk_thread_kernel).  Long
+// rows of a small batch, which would leave few warps each walking hundreds of groups, run
+// pass 1 in segments of a row (topk_seg_kernel: each segment's 16 largest scores, merged per
+// row by the bitonic merge) and, unless a row of the warp shares its threshold, pass 2 in the
+// same segments (topk_emit_kernel).
 //
 // Larger top_k (the warp kernels below): one warp per row.
 // Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
