@@ -97,6 +97,17 @@ def test_noalloc_after_larger_plan_other_top_k_quantised_and_without_status():
     _noalloc_matches(run, ref_p, ref_l, None, "small, no status word")
 
 
+def test_noalloc_long_context():
+    """16 tokens after 1,048,560 cached (8192 pages): the inversion runs its multi-kernel form
+    in the array (one scan block per eight of the 8192 buckets), and the top-k's segment lists,
+    which only topk_select uses, are not part of the array's need."""
+    w = synth.workload("custom", seed=25, q_lens=[16], ctx_lens=[1048560], num_q_heads=2,
+                       num_kv_heads=1, head_dim=64, top_k=16)
+    run, ref_p, ref_l = _workspace_reference(w)
+    status = torch.zeros(1, dtype=torch.int32, device=run.dev)
+    _noalloc_matches(run, ref_p, ref_l, status, "1M-token context")
+
+
 def test_noalloc_rejects_a_batch_larger_than_its_scratch():
     """4096 tokens x 32 heads x top-64 needs more scratch than the array holds: the call is
     refused before any launch.  Every buffer is real and of the size the arguments declare (the
