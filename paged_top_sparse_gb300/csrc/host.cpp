@@ -135,7 +135,7 @@ struct sps_plan {
           off_range_sums = 0,
           off_qconv = -1, off_kconv = -1,
           off_bucket_offsets = 0, off_entries = 0, off_fwd_tasks = 0, off_topk_lists = -1,
-          off_topk_meta = -1,
+          off_topk_meta = -1, off_topk_gmax = -1,
           ws_bytes = 0;
   int64_t fwd_ws_bytes = 0;  // the part the forward uses (the no-allocation forward's need)
   int32_t topk_nseg = 1, topk_segg = 0;
@@ -337,7 +337,9 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
   // Top-k with top_k <= 16 runs a thread per row, so long rows of a small batch leave few
   // warps, each walking hundreds of 16-page groups one after another.  From 64 groups on, pass
   // 1 is split into segments of at least 32 groups, enough of them for ~24 warps per SM of a
-  // 152-SM GPU; each segment's 16 largest scores go to this area and merge per row.
+  // 152-SM GPU; each segment's 16 largest scores go to this area and merge per row, and the
+  // largest score of each 16-page group lets pass 2 read only the groups that can hold a
+  // chosen page.
   const int64_t groups = (p.max_pages_per_req + 15) / 16;
   if (p.top_k > 1 && p.top_k <= 16 && groups >= 64) {
     const int64_t warps = (pl->R + 31) / 32, target = 24 * 152;
@@ -346,7 +348,8 @@ sps_status sparse_prefill_plan(const sps_problem* problem, sps_plan** out,
       pl->topk_nseg = (int32_t)nseg;
       pl->topk_segg = (int32_t)((groups + nseg - 1) / nseg);
       pl->off_topk_lists = take(4 * 16 * pl->R * nseg);
-      pl->off_topk_meta = take(4 * (2 + nseg) * pl->R);
+      pl->off_topk_meta = take(4 * 3 * pl->R);
+      pl->off_topk_gmax = take(4 * groups * pl->R);
     }
   }
   pl->ws_bytes = off;
@@ -431,6 +434,8 @@ DevPlan make_dev_plan(const sps_plan* pl, void* ws) {
   d.topk_lists = pl->off_topk_lists >= 0 ? reinterpret_cast<float*>(base + pl->off_topk_lists)
                                          : nullptr;
   d.topk_meta = pl->off_topk_meta >= 0 ? reinterpret_cast<int32_t*>(base + pl->off_topk_meta)
+                                       : nullptr;
+  d.topk_gmax = pl->off_topk_gmax >= 0 ? reinterpret_cast<float*>(base + pl->off_topk_gmax)
                                        : nullptr;
   d.topk_nseg = pl->topk_nseg;
   d.fwd_prefetch = pl->fwd_prefetch;

@@ -80,10 +80,11 @@ struct DevPlan {
   // top_k <= 16 over long rows: pass 1 of each row split into topk_nseg segments of topk_segg
   // 16-page groups, each segment's 16 largest scores in topk_lists [rows][topk_nseg][16]
   // (topk_nseg 1: no split, topk_lists null)
-  // and, per row, [0] 1 when pass 2 runs by segments, [1] the threshold, [2 + s] where segment
-  // s's pages start in the row's output: topk_meta [rows][2 + topk_nseg]
+  // and, per row, the rule pass 2 applies (need, then the bits of ge and eq): topk_meta
+  // [rows][3]; and the largest candidate score of each 16-page group: topk_gmax [groups][rows]
   float* topk_lists;
   int32_t* topk_meta;
+  float* topk_gmax;
   int32_t topk_nseg, topk_segg;
   // forward, BF16 K/V: when buckets hold few rows (an item of one group or less, so every group
   // waits for its own K/V tiles), the K/V tiles of the item this many items ahead are

@@ -23,8 +23,8 @@
 // (topk_tma_kernel); other layouts are read by per-thread loads (topk_thread_kernel).  Long
 // rows of a small batch, which would leave few warps each walking hundreds of groups, run
 // pass 1 in segments of a row (topk_seg_kernel: each segment's 16 largest scores, merged per
-// row by the bitonic merge) and, unless a row of the warp shares its threshold, pass 2 in the
-// same segments (topk_emit_kernel).
+// row by the bitonic merge, and each group's largest score), and pass 2 reads again only the
+// groups whose largest score reaches the row's threshold (topk_emit_rows_kernel).
 //
 // Larger top_k (the warp kernels below): one warp per row.
 // Scores become 32-bit order-preserving keys.  Lane l holds the E adjacent pages E l .. E l + E-1,
@@ -117,9 +117,9 @@ __device__ __forceinline__ void load_group(const float* row, int base, int o, fl
 }
 
 // Pass 1 of a row: the scores of pages base .. base+15 that lie below o join the running list
-// of the 16 largest.
-__device__ __forceinline__ void take_group(float (&best)[16], const float4 (&f)[4], int base,
-                                           int o) {
+// of the 16 largest.  Returns the largest of them.
+__device__ __forceinline__ float take_group(float (&best)[16], const float4 (&f)[4], int base,
+                                            int o) {
   float g[16];
   if (base + 16 <= o) {  // a full group: every page is a candidate
 #pragma unroll
@@ -141,6 +141,7 @@ __device__ __forceinline__ void take_group(float (&best)[16], const float4 (&f)[
   }
   sort16_desc(g);
   merge16_desc(best, g);
+  return g[0];
 }
 
 // The selection rule read off the list (o >= K >= 2 candidates, so the (K-1)-th and K-th
@@ -346,8 +347,9 @@ __device__ __forceinline__ void load_list(const float* src, float (&g)[16]) {
 
 // Pass 1 of long rows split into segments (DevPlan::topk_nseg): warp w of block (x, y) runs
 // pass 1 of its 32 rows over the 16-page groups [y * segg, (y + 1) * segg), through the same
-// per-warp tile ring, and stores each full row's 16 largest scores of the segment (descending)
-// to topk_lists[row][y]; a segment past a row's last candidate stores nothing.
+// per-warp tile ring, stores each full row's 16 largest scores of the segment (descending) to
+// topk_lists[row][y] (a segment past a row's last candidate stores nothing) and the largest
+// candidate score of each of its groups to topk_gmax[group][row].
 template <int S>
 __global__ void __launch_bounds__(256)
 topk_seg_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p) {
@@ -397,7 +399,7 @@ topk_seg_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p) {
     if (full && base < o) {
       float4 f[4];
       topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
-      take_group(best, f, base, o);
+      p.topk_gmax[(int64_t)(g0 + n) * R + r] = take_group(best, f, base, o);
     }
     __syncwarp();
     if (lane == 0 && n + S < items)
@@ -416,88 +418,125 @@ topk_seg_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p) {
   }
 }
 
-// Pass 2 of long rows by segments, after topk_tma_kernel<S, true> left it to this kernel
-// (topk_meta[row][0] = 1): warp w of block (x, y) walks its rows' groups of segment y and
-// writes the pages at or above the row's threshold, in order, from the segment's start in the
-// row's output on.  The own page (slot k-1) and every other row were written by that kernel.
-template <int S>
-__global__ void __launch_bounds__(256)
-topk_emit_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + 8 * S * kTopkTile);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t my_tiles = smem_u32(tiles + warp * S * kTopkTile);
-  const uint32_t my_bars = smem_u32(bars + warp * S);
-  if (lane == 0) {
-    tma_prefetch_desc(&tmS);
-    for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  pdl_wait();  // the row kernel's thresholds and offsets
-  const int64_t R = (int64_t)p.T * p.H;
-  const int64_t r0 = (int64_t)blockIdx.x * 256 + warp * 32;
-  if (r0 >= R) return;  // warp-uniform; this warp issued no copy
-  const int64_t r = r0 + lane;
-  const int K = p.K, nseg = p.topk_nseg;
-  const int g0 = (int)blockIdx.y * p.topk_segg;
-  int o = 0, off = 0;
-  float ge = 0.f;
-  bool act = false;
-  if (r < R) {
-    o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
-    if (o >= K && K > 1 && 16 * g0 < o) {
-      const int32_t* meta = p.topk_meta + r * (2 + nseg);
-      act = meta[0] == 1;
-      ge = __int_as_float(meta[1]);
-      off = meta[2 + blockIdx.y];
-    }
-  }
-  const int Gw = (int)__reduce_max_sync(0xffffffffu, act ? (uint32_t)(o + 15) / 16u : 0u);
-  const int g1 = min(Gw, g0 + p.topk_segg);
-  const int items = g1 > g0 ? g1 - g0 : 0;
-  if (lane == 0)
-    for (int n = 0; n < S && n < items; ++n)
-      topk_issue_group<S>(&tmS, my_tiles, my_bars, n, g0 + n, (int)r0);
-  int32_t* out = idx + r * K;
-  bool ok = true;
-  for (int n = 0; n < items; ++n) {
-    const int s = n % S;
-    if (!topk_tile_ready<S>(my_bars + 8 * s, n, p.status)) {
-      ok = false;
-      break;
-    }
-    const int base = 16 * (g0 + n);
-    if (act && base < o) {
-      float4 f[4];
-      topk_read_tile(tiles + (warp * S + s) * kTopkTile, lane, f);
-      const float v[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
-                           f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
-      uint32_t bits = 0u;
+// Pass 2 of long rows after topk_tma_kernel<S, true> (rows of 16-byte pitch), eight threads
+// per row, each over one eighth of the row's 16-page groups in page order: of its groups only
+// those whose largest candidate reaches the threshold (topk_gmax: a taken page, or a page
+// equal to the threshold, lies in no other) are read.  A first walk counts the pages each
+// thread takes (those above the threshold, and of those equal to it as many as the row still
+// needs, lowest pages first); a prefix over the eight gives each its start in the row's
+// output, and a second walk writes them.
+constexpr int kEmitSub = 8;  // threads per row
+
+// Groups g0 .. g1-1 of a row whose largest candidate reaches thr, in order: f(g).
+template <typename F>
+__device__ __forceinline__ void for_hit_groups(const DevPlan& p, int64_t R, int64_t r, int g0,
+                                               int g1, float thr, F&& f) {
+  for (int b = g0; b < g1; b += 8) {  // eight group maxima in flight, then the hits in order
+    float gm[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) bits |= v[e] >= ge ? 1u << e : 0u;
-      if (o - base < 16) bits &= (1u << (o - base)) - 1u;
-      while (bits) {
-        if (off < K - 1) out[off] = base + __ffs(bits) - 1;  // in bounds whatever the scores
-        ++off;
-        bits &= bits - 1u;
-      }
+    for (int u = 0; u < 8; ++u)
+      gm[u] = b + u < g1 ? __ldcg(p.topk_gmax + (int64_t)(b + u) * R + r) : -INFINITY;
+    uint32_t hit = 0u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) hit |= gm[u] >= thr ? 1u << u : 0u;
+    while (hit) {
+      f(b + __ffs(hit) - 1);
+      hit &= hit - 1u;
     }
-    __syncwarp();
-    if (lane == 0 && n + S < items)
-      topk_issue_group<S>(&tmS, my_tiles, my_bars, n + S, g0 + n + S, (int)r0);
-  }
-  if (!ok) {  // let the copies already issued land before the block's shared memory is reused
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < kSettleNs) __nanosleep(1000);
   }
 }
 
-// SEG: pass 1 comes from topk_seg_kernel's per-segment lists, merged here; the tile sequence
-// is pass 2 alone, and only for warps with a row whose threshold is shared (the others leave
-// pass 2 to topk_emit_kernel).
+__global__ void __launch_bounds__(256)
+topk_emit_rows_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
+                      int32_t* __restrict__ idx) {
+  pdl_wait();  // the rows' rules from the kernel before
+  const int64_t R = (int64_t)p.T * p.H;
+  const int64_t r = (int64_t)blockIdx.x * (256 / kEmitSub) + threadIdx.x / kEmitSub;
+  const int sub = threadIdx.x % kEmitSub;
+  const int K = p.K;
+  bool full = false;
+  int o = 0;
+  if (r < R) {
+    o = __ldg(p.tok_pos + (uint32_t)r / (uint32_t)p.H) >> 7;
+    full = o >= K && K > 1;  // other rows were written whole by the kernel before
+  }
+  int need = 0;
+  float ge = 0.f, eq = 0.f;
+  if (full) {
+    const int32_t* meta = p.topk_meta + r * 3;
+    need = meta[0];
+    ge = __int_as_float(meta[1]);
+    eq = __int_as_float(meta[2]);
+  }
+  const float thr = need > 0 ? eq : ge;
+  const float* row = scores + r * pitch;
+  const int G = (o + 15) / 16, per = (G + kEmitSub - 1) / kEmitSub;
+  const int g0 = min(G, sub * per), g1 = min(G, g0 + per);
+  // walk 1: the pages above the threshold (need 0: at or above it) and those equal to it
+  int above = 0, equal = 0;
+  if (full)
+    for_hit_groups(p, R, r, g0, g1, thr, [&](int g) {
+      float4 f[4];
+      load_group<true>(row, 16 * g, o, f);
+      const float v[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
+                           f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
+      const int nb = o - 16 * g < 16 ? o - 16 * g : 16;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (e < nb) {
+          above += (need > 0 ? v[e] > eq : v[e] >= ge) ? 1 : 0;
+          equal += need > 0 && v[e] == eq ? 1 : 0;
+        }
+      }
+    });
+  // the equal pages of lower threads come first; then this thread's start in the output
+  int eq_before = equal;
+#pragma unroll
+  for (int d = 1; d < kEmitSub; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, eq_before, d, kEmitSub);
+    if (sub >= d) eq_before += y;
+  }
+  eq_before -= equal;
+  int my_eq = need - eq_before;
+  my_eq = my_eq < 0 ? 0 : (my_eq > equal ? equal : my_eq);
+  int start = above + my_eq;
+#pragma unroll
+  for (int d = 1; d < kEmitSub; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, start, d, kEmitSub);
+    if (sub >= d) start += y;
+  }
+  start -= above + my_eq;
+  // walk 2: write them
+  int32_t* out = idx + r * K;
+  if (full) {
+    int pos = start;
+    for_hit_groups(p, R, r, g0, g1, thr, [&](int g) {
+      float4 f[4];
+      load_group<true>(row, 16 * g, o, f);
+      const float v[16] = {f[0].x, f[0].y, f[0].z, f[0].w, f[1].x, f[1].y, f[1].z, f[1].w,
+                           f[2].x, f[2].y, f[2].z, f[2].w, f[3].x, f[3].y, f[3].z, f[3].w};
+      const int nb = o - 16 * g < 16 ? o - 16 * g : 16;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (e < nb) {
+          bool take = need > 0 ? v[e] > eq : v[e] >= ge;
+          if (need > 0 && v[e] == eq && my_eq > 0) {
+            take = true;
+            --my_eq;
+          }
+          if (take) {
+            if (pos < K - 1) out[pos] = 16 * g + e;  // in bounds whatever the scores
+            ++pos;
+          }
+        }
+      }
+    });
+    if (sub == 0) out[K - 1] = o;
+  }
+}
+
+// SEG: pass 1 comes from topk_seg_kernel's per-segment lists, merged here into each row's rule
+// for topk_emit_rows_kernel; this kernel then writes the short rows (and the own page) only.
 template <int S, bool SEG>
 __global__ void __launch_bounds__(256)
 topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __restrict__ idx) {
@@ -536,43 +575,23 @@ topk_tma_kernel(const __grid_constant__ CUtensorMap tmS, DevPlan p, int32_t* __r
   TopkRule rule{};
   bool ok = true;
   int pos = 0;
-  bool walk = true;  // SEG: this warp runs pass 2 itself
-  if (SEG) {
-    // pass 1 from the segments' lists (descending), merged; then, unless some row of the warp
-    // shares its threshold, every full row leaves pass 2 to topk_emit_kernel: its threshold
-    // and, per segment, where the segment's pages start in the row's output (the count of
-    // earlier lists' entries at or above the threshold: with the threshold not shared, exactly
-    // k - 1 candidates reach it, and each lies in its segment's list)
+  if (SEG && full) {
+    // pass 1 from the segments' lists (descending), merged; the rule for topk_emit_rows_kernel,
+    // which runs pass 2
     const int nseg = p.topk_nseg;
-    if (full) {
-      for (int sg = 0; sg < nseg && 16 * sg * p.topk_segg < o; ++sg) {
-        float g[16];
-        load_list(p.topk_lists + (r * nseg + sg) * 16, g);
-        merge16_desc(best, g);
-      }
-      rule = selection_rule(best, K);
+    for (int sg = 0; sg < nseg && 16 * sg * p.topk_segg < o; ++sg) {
+      float g[16];
+      load_list(p.topk_lists + (r * nseg + sg) * 16, g);
+      merge16_desc(best, g);
     }
-    walk = __any_sync(0xffffffffu, full && rule.need > 0);
-    if (full) {
-      int32_t* meta = p.topk_meta + r * (2 + nseg);
-      meta[0] = walk ? 0 : 1;
-      meta[1] = __float_as_int(rule.ge);
-      if (!walk) {
-        int acc = 0;
-        for (int sg = 0; sg < nseg; ++sg) {
-          meta[2 + sg] = acc;
-          if (16 * sg * p.topk_segg < o) {
-            float g[16];
-            load_list(p.topk_lists + (r * nseg + sg) * 16, g);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc += g[i] >= rule.ge ? 1 : 0;
-          }
-        }
-      }
-    }
+    rule = selection_rule(best, K);
+    int32_t* meta = p.topk_meta + r * 3;
+    meta[0] = rule.need;
+    meta[1] = __float_as_int(rule.ge);
+    meta[2] = __float_as_int(rule.eq);
   }
   const int p2 = SEG ? 0 : G;  // first item of pass 2
-  const int items = SEG && !walk ? 0 : p2 + G;
+  const int items = SEG ? 0 : p2 + G;
   if (lane == 0)
     for (int n = 0; n < S && n < items; ++n)
       topk_issue_tile<S>(&tmS, my_tiles, my_bars, n, G, (int)r0);
@@ -855,9 +874,11 @@ topk_filter_kernel(DevPlan p, const float* __restrict__ scores, int64_t pitch,
 }  // namespace
 
 template <int S>
-cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, int32_t* idx, unsigned grid,
-                            cudaStream_t st) {
-  if (p.topk_nseg > 1 && p.topk_lists) {  // long rows: pass 1 by segments, then the merge
+cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, const float* scores,
+                            int64_t pitch, int32_t* idx, unsigned grid, cudaStream_t st) {
+  if (p.topk_nseg > 1 && p.topk_lists) {
+    // long rows: pass 1 by segments, the merge into each row's rule, pass 2 per row over the
+    // groups that can hold a chosen page
     cudaError_t e = cudaFuncSetAttribute(topk_seg_kernel<S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)topk_smem<S>());
@@ -871,11 +892,10 @@ cudaError_t launch_topk_tma(const CUtensorMap& tm, const DevPlan& p, int32_t* id
     e = launch_pdl(topk_tma_kernel<S, true>, dim3(grid), dim3(256), topk_smem<S>(), st, tm, p,
                    idx);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_emit_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)topk_smem<S>());
-    if (e != cudaSuccess) return e;
-    return launch_pdl(topk_emit_kernel<S>, dim3(grid, (unsigned)p.topk_nseg), dim3(256),
-                      topk_smem<S>(), st, tm, p, idx);
+    const int64_t R = (int64_t)p.T * p.H, rows_per_block = 256 / kEmitSub;
+    return launch_pdl(topk_emit_rows_kernel,
+                      dim3((unsigned)((R + rows_per_block - 1) / rows_per_block)), dim3(256), 0,
+                      st, p, scores, pitch, idx);
   }
   cudaError_t e = cudaFuncSetAttribute(topk_tma_kernel<S, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -899,8 +919,8 @@ cudaError_t launch_topk(const DevPlan& p, const float* scores, int64_t pitch, in
                                 (uint64_t)pitch * 4, 16, 32)) {
       // rows of many groups need a deeper ring per warp to cover the tile latency (4 stages: two
       // blocks per SM); short rows do better with three blocks per SM (3 stages)
-      if (p.max_pages <= 128) e = launch_topk_tma<3>(tm, p, idx, grid, st);
-      else e = launch_topk_tma<4>(tm, p, idx, grid, st);
+      if (p.max_pages <= 128) e = launch_topk_tma<3>(tm, p, scores, pitch, idx, grid, st);
+      else e = launch_topk_tma<4>(tm, p, scores, pitch, idx, grid, st);
     } else if (vec) {
       e = launch_pdl(topk_thread_kernel<true>, dim3(grid), dim3(256), 0, st, p, scores, pitch, idx);
     } else {
