@@ -13,8 +13,9 @@ form (copy in, step, copy out, one after another) is reported beside it.
 The default line (the 8K BF16 prefill with FP32 partials) also carries, under ``configs``, the
 same measurement of every other configuration of the method's workloads: the 8K prefill with
 FP16 and with BF16 partials, the quantised 8K prefill (exact route and the FP8 route), the
-combine stress (a 4.3 GB FP32 partial buffer) and the chunked batch (8 x 512 new tokens over
-~32K of context); ``--no-configs`` skips them.
+combine stress (a 4.3 GB FP32 partial buffer), the chunked batch (8 x 512 new tokens over
+~32K of context) and 512 new tokens at the end of a 1M-token context; ``--no-configs`` skips
+them.
 
 ``--impl reference`` times the FP64 CPU oracle instead (a bounded row sample per step).
 
@@ -575,7 +576,8 @@ def _sub(line):
 def run_other_configs(args, world, w0, t0):
     """Every other configuration of the method's workloads, each timed like the headline:
     the 8K prefill with 16-bit partials (FP16, BF16), the quantised 8K prefill (exact route
-    and the FP8 route), the combine stress and the chunked 8 x 512-over-32K batch."""
+    and the FP8 route), the combine stress, the chunked 8 x 512-over-32K batch and 512 new
+    tokens at the end of a 1M-token context."""
     import torch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -597,6 +599,9 @@ def run_other_configs(args, world, w0, t0):
     torch.cuda.empty_cache()
     line, _, _ = run_prefill(args, world, dev, "chunked32k")
     out["chunked32k"] = _sub(line)
+    torch.cuda.empty_cache()
+    line, _, _ = run_prefill(args, world, dev, "ctx1m")
+    out["ctx1m"] = _sub(line)
     torch.cuda.empty_cache()
     return out
 
