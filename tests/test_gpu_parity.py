@@ -235,6 +235,33 @@ def test_topk_long_rows_by_segments(k):
     assert bad.size == 0, f"{bad.size} rows differ, first {bad[:5]}"
 
 
+def test_topk_long_and_short_rows_in_one_warp():
+    """A plan whose long request (5469 pages) splits the top-k into segments, with a second
+    request of one or two pages: the first warp holds 24 long rows and 8 short ones (fewer
+    visible pages than k: every page, then -1), so the segment kernels skip rows the row kernel
+    writes whole."""
+    from paged_top_sparse_gb300 import binding as B
+
+    w = synth.workload("custom", seed=26, q_lens=[6, 40], ctx_lens=[700000, 100], num_q_heads=4,
+                       num_kv_heads=2, head_dim=128, top_k=16)
+    plan = B.Plan(w.q_lens, w.ctx_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.top_k,
+                  w.max_pages, w.num_phys_pages)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda:0")
+    B.sps_plan_upload(plan, ws)
+    rng = np.random.default_rng(8)
+    R, P = w.num_rows, w.max_pages
+    s = rng.standard_normal((R, P)).astype(np.float32)
+    _, tok_pos = orc.token_meta(oracle_problem(w))
+    own = (tok_pos[np.arange(R) // w.num_q_heads] // 128)[:, None]
+    s[np.arange(P)[None, :] > own] = np.nan
+    idx = torch.full((R, w.top_k), -7, dtype=torch.int32, device="cuda:0")
+    B.topk_select(plan, torch.from_numpy(s).cuda(), idx, ws)
+    torch.cuda.synchronize()
+    assert B.sps_read_device_status(plan, ws) == 0
+    ref = orc.topk(oracle_problem(w), np.nan_to_num(s.astype(np.float64), nan=-np.inf))
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("pad", [0, 1, 4])
 @pytest.mark.parametrize("q_lens,ctx_lens,k", [
     ([150, 90, 301], [2100, 700, 0], 16),  # three requests: rows of a warp see different pages
