@@ -489,7 +489,7 @@ def test_combine_bf16_direct(D, S, R, pad):
 
 
 P16_WORKLOADS = ["tiny", "ragged", "mha_d64", "k1", "quant_small", "chunked_fp8_small",
-                 "prefill8k"]
+                 "ctx1m", "prefill8k"]
 
 
 @pytest.mark.parametrize("storage", ["f16", "bf16"])
